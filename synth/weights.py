@@ -1,0 +1,153 @@
+"""Seeded synthetic weights in the canonical host format.
+
+Draws (the synthetic workloads' recipe):
+  * bf16 tensors (every linear of the bf16 model, the token embedding, the per-layer
+    embedding table): N(0, std) drawn in fp32, rounded to bf16 round-to-nearest-even.
+  * W4A16 linears: q ~ uniform integers in [-8, 7]; scale = bf16(|N(0, scale_std)|), one per
+    32 input values; packed eight nibbles per int32, low nibble first.
+  * RMSNorm gains: bf16(1 + N(0, gain_std)), i.e. exactly 1 at gain_std = 0.
+  * layer scales: 1 + N(0, layer_scale_std) in fp32 (exactly 1 at std 0).
+
+Each tensor has its own stream, SeedSequence([seed, tensor id, chunk]), so tensors are
+independent of the order in which they are drawn and large tensors fill in parallel.
+"""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from .configs import layer_is_full, layer_mlp_width
+
+_CHUNK = 1 << 22
+_LINEARS = ("q", "k", "v", "o", "gate", "up", "down", "ple_gate", "ple_proj")
+_LAYER_NORMS = ("in_norm", "post_attn_norm", "pre_ffw_norm", "post_ffw_norm", "post_ple_norm")
+
+
+def bf16_from_f32(a):
+    """fp32 array -> bf16 bit patterns (uint16), round to nearest even (finite inputs)."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    bits = a.view(np.uint32)
+    rounded = bits + np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1))
+    return (rounded >> np.uint32(16)).astype(np.uint16)
+
+
+def _pool():
+    return ThreadPoolExecutor(max(1, len(os.sched_getaffinity(0))))
+
+
+def _chunked(n, seed, tid, fill, out, pool):
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+
+    def work(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tid, c])))
+        out[lo:hi] = fill(rng, hi - lo)
+
+    list(pool.map(work, range(nchunks)))
+
+
+def _normal_bf16(shape, std, seed, tid, pool):
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16)
+
+    def fill(rng, m):
+        a = rng.standard_normal(m, dtype=np.float32)
+        a *= np.float32(std)
+        return bf16_from_f32(a)
+
+    _chunked(n, seed, tid, fill, out, pool)
+    return out.reshape(shape)
+
+
+def _gain_bf16(n, std, seed, tid, pool):
+    if std == 0.0:
+        return np.full(n, 0x3F80, np.uint16)          # bf16 1.0
+    g = _normal_bf16((n,), std, seed, tid, pool).astype(np.uint32) << np.uint32(16)
+    return bf16_from_f32(np.float32(1.0) + g.view(np.float32))
+
+
+def _int4_linear(n_out, n_in, scale_std, seed, tid, pool):
+    assert n_in % 32 == 0
+    q = np.empty(n_out * n_in, np.int8)
+    _chunked(q.size, seed, tid, lambda rng, m: rng.integers(-8, 8, m, dtype=np.int8), q, pool)
+    nib = (q.reshape(n_out, n_in // 8, 8).astype(np.uint32) & np.uint32(0xF))
+    shifts = (np.arange(8, dtype=np.uint32) * np.uint32(4))
+    packed = np.bitwise_or.reduce(nib << shifts, axis=2).view(np.int32)
+    s = np.empty(n_out * (n_in // 32), np.uint16)
+
+    def fill(rng, m):
+        a = np.abs(rng.standard_normal(m, dtype=np.float32))
+        a *= np.float32(scale_std)
+        return bf16_from_f32(a)
+
+    _chunked(s.size, seed, tid + 50_000, fill, s, pool)
+    return {"packed": np.ascontiguousarray(packed), "scales": s.reshape(n_out, n_in // 32),
+            "shape": (n_out, n_in)}
+
+
+def linear_names():
+    return _LINEARS
+
+
+def linear_shapes(cfg, layer):
+    """(N, K) of every linear stored for a layer of the synthetic checkpoint."""
+    H, P = cfg["hidden"], cfg["ple_dim"]
+    d = cfg["head_dim_full"] if layer_is_full(cfg, layer) else cfg["head_dim_sliding"]
+    F = layer_mlp_width(cfg, layer)
+    nq = cfg["num_q_heads"] * d
+    return {"q": (nq, H), "k": (d, H), "v": (d, H), "o": (H, nq), "gate": (F, H),
+            "up": (F, H), "down": (H, F), "ple_gate": (P, H), "ple_proj": (H, P)}
+
+
+def make_weights(cfg, fmt, seed=0, std=0.02, scale_std=0.004, gain_std=0.0,
+                 layer_scale_std=0.0, embed_std=None):
+    """Draw every tensor of the synthetic checkpoint.
+
+    fmt: "bf16" (every linear bf16) or "w4a16" (linears int4 + bf16 group scales; the token
+    embedding and per-layer-embedding table stay bf16).  K and V projections are drawn for
+    every layer, as a checkpoint that carries them everywhere would; a decoder reads those
+    of the layers that compute their own K/V.
+    """
+    assert fmt in ("bf16", "w4a16")
+    L, H, P, V = cfg["num_layers"], cfg["hidden"], cfg["ple_dim"], cfg["vocab"]
+    estd = std if embed_std is None else embed_std
+    with _pool() as pool:
+        def linear(n_out, n_in, tid):
+            if fmt == "bf16":
+                return {"w": _normal_bf16((n_out, n_in), std, seed, tid, pool),
+                        "shape": (n_out, n_in)}
+            return _int4_linear(n_out, n_in, scale_std, seed, tid, pool)
+
+        w = {"fmt": fmt,
+             "embed": _normal_bf16((V, H), estd, seed, 1, pool),
+             "ple_table": _normal_bf16((V, L * P), estd, seed, 2, pool),
+             "ple_model_proj": linear(L * P, H, 3),
+             "ple_proj_norm": _gain_bf16(P, gain_std, seed, 4, pool),
+             "final_norm": _gain_bf16(H, gain_std, seed, 5, pool),
+             "layers": []}
+        for l in range(L):
+            base = 1000 + 64 * l
+            shapes = linear_shapes(cfg, l)
+            lw = {}
+            for i, name in enumerate(_LINEARS):
+                lw[name] = linear(*shapes[name], base + i)
+            for i, name in enumerate(_LAYER_NORMS):
+                lw[name] = _gain_bf16(H, gain_std, seed, base + 20 + i, pool)
+            d = shapes["k"][0]
+            lw["q_norm"] = _gain_bf16(d, gain_std, seed, base + 30, pool)
+            lw["k_norm"] = _gain_bf16(d, gain_std, seed, base + 31, pool)
+            if layer_scale_std == 0.0:
+                lw["layer_scale"] = 1.0
+            else:
+                rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, base + 40])))
+                lw["layer_scale"] = float(np.float32(1.0 + layer_scale_std * rng.standard_normal()))
+            w["layers"].append(lw)
+    return w
+
+
+def iter_linears(weights):
+    """(name, linear) for every linear tensor of a weight dict, in a fixed order."""
+    yield "ple_model_proj", weights["ple_model_proj"]
+    for l, lw in enumerate(weights["layers"]):
+        for name in _LINEARS:
+            yield f"layers.{l}.{name}", lw[name]

@@ -1,0 +1,233 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix (CPU only).
+
+Each test checks the oracle against something other than itself: a printed number, a
+closed form, an invariant, a special case reducing to a textbook result, or brute force."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _pack_row(q):
+    """Hand packing of one row of int4 values in the canonical layout (low nibble first)."""
+    words = []
+    for w in range(len(q) // 8):
+        v = 0
+        for j in range(8):
+            v |= (int(q[8 * w + j]) & 0xF) << (4 * j)
+        words.append(v)
+    return np.array(words, dtype=np.uint32).view(np.int32)
+
+
+def _bf16(x):
+    return np.array([x], np.float32).view(np.uint32)[0] >> 16
+
+
+# ---------------------------------------------------------------------------------- dequant
+def test_dequant_levels_exact():
+    # q = -8..7 twice, scale 0.5: every product is exactly representable.
+    q = np.array(list(range(-8, 8)) * 2)
+    packed = _pack_row(q)[None]
+    scales = np.array([[_bf16(0.5)]], np.uint16)
+    w = oracle.dequant_w4a16(packed, scales)
+    np.testing.assert_array_equal(w[0], q * 0.5)
+
+
+def test_dequant_nibble_order_probe():
+    # One non-zero nibble at each position k: exactly element k is non-zero.
+    for k in range(32):
+        q = np.zeros(32, int)
+        q[k] = 3
+        w = oracle.dequant_w4a16(_pack_row(q)[None], np.array([[_bf16(1.0)]], np.uint16))
+        assert np.nonzero(w[0])[0].tolist() == [k]
+        assert w[0, k] == 3.0
+
+
+def test_dequant_extreme_levels_and_group_scales():
+    # Groups whose largest weight sits on level 7 or -8 (the QAT grid's two top levels),
+    # each group with its own scale.
+    q = np.array([7] * 32 + [-8] * 32)
+    scales = np.array([[_bf16(0.25), _bf16(3.0)]], np.uint16)
+    w = oracle.dequant_w4a16(_pack_row(q)[None], scales)
+    assert np.all(w[0, :32] == 1.75) and np.all(w[0, 32:] == -24.0)
+
+
+def test_dequant_rounds_to_bf16_nearest_even():
+    # s = 1 + 1/128, q = 3: 3.0234375 lies exactly between bf16 3.015625 and 3.03125 -> even (3.03125)
+    # s = 1 + 3/128, q = 3: 3.0703125 between 3.0625 and 3.078125 -> even (3.0625)
+    # s = 1 + 1/128, q = 5: 5.0390625 -> below the midpoint -> 5.03125
+    # s = 1 + 3/128, q = -3: symmetric -> -3.0625
+    # s = 1 + 127/128, q = 7: 13.9453125, bf16 spacing 1/16 there -> 13.9375
+    cases = [(3, 1 + 1 / 128, 3.03125), (3, 1 + 3 / 128, 3.0625), (5, 1 + 1 / 128, 5.03125),
+             (-3, 1 + 3 / 128, -3.0625), (7, 1 + 127 / 128, 13.9375)]
+    for q, s, want in cases:
+        row = np.zeros(32, int)
+        row[0] = q
+        w = oracle.dequant_w4a16(_pack_row(row)[None], np.array([[_bf16(s)]], np.uint16))
+        assert w[0, 0] == want, (q, s, w[0, 0], want)
+
+
+def test_bf16_round_fp32_and_fp64_agree_on_exact_inputs():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(10000).astype(np.float32)
+    a = oracle.bf16_round(x).astype(np.float64)
+    b = oracle.bf16_round(x.astype(np.float64))
+    np.testing.assert_array_equal(a, b)
+    # Result is a bf16 value: low 16 bits zero; and the nearest one.
+    bits = oracle.bf16_round(x).view(np.uint32)
+    assert np.all((bits & 0xFFFF) == 0)
+    assert np.all(np.abs(oracle.bf16_round(x) - x) <= np.abs(x) * 2.0 ** -8)
+
+
+# ---------------------------------------------------------------------------------- rmsnorm
+def test_rmsnorm_constant_and_hand_case():
+    g = np.array([1.0, 2.0, 0.5, -1.0], np.float64)
+    out = oracle.rmsnorm(np.full(4, -3.0), g, 0.0)
+    np.testing.assert_allclose(out, -g, rtol=1e-15)
+    # [3, 4]: mean square 12.5
+    out = oracle.rmsnorm(np.array([3.0, 4.0]), np.ones(2), 0.0)
+    np.testing.assert_allclose(out, [3 / math.sqrt(12.5), 4 / math.sqrt(12.5)], rtol=1e-15)
+    # eps enters under the square root: a zero vector stays zero, a tiny one is damped
+    assert np.all(oracle.rmsnorm(np.zeros(8), np.ones(8), 1e-6) == 0)
+    np.testing.assert_allclose(oracle.rmsnorm(np.full(2, 1e-3), np.ones(2), 1e-6),
+                               1e-3 / math.sqrt(1e-6 + 1e-6), rtol=1e-12)
+
+
+def test_rmsnorm_scale_invariance():
+    rng = np.random.default_rng(2)
+    v = rng.standard_normal((3, 64))
+    g = rng.standard_normal(64)
+    np.testing.assert_allclose(oracle.rmsnorm(v * 37.5, g, 0.0), oracle.rmsnorm(v, g, 0.0),
+                               rtol=1e-12)
+
+
+# ------------------------------------------------------------------------------------- gelu
+def test_gelu_tanh_identities():
+    from scipy.special import erf
+    z = np.linspace(-8, 8, 4001)
+    g = oracle.gelu_tanh(z)
+    # odd-part identity of x * Phi~(x) with Phi~(x) + Phi~(-x) = 1
+    np.testing.assert_allclose(g - oracle.gelu_tanh(-z), z, atol=1e-12)
+    # within the tanh form's known approximation error of the erf GELU
+    exact = 0.5 * z * (1 + erf(z / math.sqrt(2)))
+    assert np.max(np.abs(g - exact)) < 1e-3
+    assert oracle.gelu_tanh(np.array([0.0]))[0] == 0.0
+    np.testing.assert_allclose(oracle.gelu_tanh(np.array([20.0, -20.0])), [20.0, 0.0], atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------- rope
+def test_rope_identity_norm_and_relative_position():
+    d = 16
+    cos, sin = oracle.rope_tables(10000.0, d, 64, np.float64)
+    rng = np.random.default_rng(3)
+    q, k = rng.standard_normal(d), rng.standard_normal(d)
+    np.testing.assert_allclose(oracle.apply_rope(q, cos[0], sin[0]), q, rtol=0, atol=0)
+    for p in (1, 7, 63):
+        r = oracle.apply_rope(q, cos[p], sin[p])
+        h = d // 2
+        np.testing.assert_allclose(r[:h] ** 2 + r[h:] ** 2, q[:h] ** 2 + q[h:] ** 2, rtol=1e-12)
+    dots = [oracle.apply_rope(q, cos[m], sin[m]) @ oracle.apply_rope(k, cos[m - 5], sin[m - 5])
+            for m in (5, 20, 40)]
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-10)
+
+
+def test_rope_is_complex_rotation():
+    # Pair (i, i + d/2) of a unit vector rotates by angle p * theta^(-2i/d).
+    d, theta = 8, 100.0
+    cos, sin = oracle.rope_tables(theta, d, 10, np.float64)
+    for i in range(d // 2):
+        v = np.zeros(d)
+        v[i] = 1.0
+        r = oracle.apply_rope(v, cos[9], sin[9])
+        ang = 9 * theta ** (-2.0 * i / d)
+        assert abs(r[i] - math.cos(ang)) < 1e-12 and abs(r[i + d // 2] - math.sin(ang)) < 1e-12
+
+
+# ---------------------------------------------------------------------------- masks / attend
+@pytest.mark.parametrize("window", [1, 2, 3, 15, 16, 17])
+def test_visible_keys_brute_force(window):
+    T = 16
+    for full in (False, True):
+        dense = np.zeros((T, T), bool)
+        for i in range(T):                      # brute force: every (query, key) pair
+            for j in range(T):
+                dense[i, j] = j <= i and (full or i - j < window)
+        for p in range(T):
+            got = np.zeros(T, bool)
+            got[oracle.visible_keys(p, full, window)] = True
+            assert np.array_equal(got, dense[p]), (p, full, window)
+
+
+def test_attend_special_cases():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((4, 8))
+    K = rng.standard_normal((1, 8))
+    V = rng.standard_normal((1, 8))
+    np.testing.assert_allclose(oracle.attend(q, K, V, 0.3), np.repeat(V, 4, 0), rtol=1e-15)
+    K = rng.standard_normal((9, 8))
+    V = rng.standard_normal((9, 8))
+    np.testing.assert_allclose(oracle.attend(np.zeros((4, 8)), K, V, 1.0),
+                               np.repeat(V.mean(0, keepdims=True), 4, 0), rtol=1e-13)
+    # one dominant key
+    K = np.zeros((5, 8))
+    K[2, 0] = 1.0
+    qq = np.zeros((1, 8))
+    qq[0, 0] = 1e4
+    np.testing.assert_allclose(oracle.attend(qq, K, V[:5], 1.0)[0], V[2], rtol=1e-12)
+
+
+# ---------------------------------------------------------------------- schedule / sharing
+def test_kv_share_map_e2b_literal():
+    cfg = synth.get_config("e2b")
+    want = list(range(15)) + [13, 13, 13, 13, 14] * 4
+    assert oracle.kv_share_map(cfg) == want
+    types = oracle.layer_types(cfg)
+    assert [l for l, t in enumerate(types) if t == "full"] == [4, 9, 14, 19, 24, 29, 34]
+    assert [oracle.mlp_width(cfg, l) for l in range(35)] == [6144] * 15 + [12288] * 20
+    own = oracle.owns_kv(cfg)
+    assert sum(own) == 15 and sum(o for o, t in zip(own, types) if t == "full") == 3
+
+
+def test_kv_share_map_tiny_readings():
+    assert oracle.kv_share_map(synth.get_config("tiny")) == [0, 1, 2, 2, 4]
+    assert oracle.kv_share_map(synth.get_config("tiny10")) == [0, 1, 2, 3, 4, 5, 5, 5, 5, 4]
+
+
+def test_printed_sizes_e2b():
+    gold = json.load(open(os.path.join(GOLD, "e2b_printed_sizes.json")))
+    cfg = synth.get_config("e2b")
+    c = oracle.param_counts(cfg)
+    assert c["n_linears"] == gold["packed_int4_linears"]["value"]
+    # linears + embedding + table in bf16 fall short of the printed total by the norm gains
+    short = gold["bf16_weight_bytes"]["value"] - c["bf16_bytes"]
+    assert 0 <= short < 1_000_000, short
+    assert round(c["w4a16_bytes"] / 1e9, 3) == gold["w4a16_weight_gb"]["value"]
+    assert round(c["embed_bytes"] / 1e9, 3) == gold["lm_head_copy_gb"]["value"]
+    assert round(c["ple_bytes"] / 1e9, 2) == gold["ple_table_gb"]["value"]
+    assert oracle.kv_bytes_per_token(cfg) == gold["kv_bytes_per_token"]["value"]
+    assert oracle.kv_bytes_per_token(cfg) // 2 == gold["kv_elements_per_token"]["value"]
+    assert 256 * oracle.kv_bytes_per_token(cfg) == gold["cache_bytes_context_256"]["value"]
+    assert oracle.kv_bytes_per_token(cfg, True) == gold["kv_cell_bytes_copy_every_layer"]["value"]
+    assert sum(oracle.owns_kv(cfg)) == gold["kv_owning_layers"]["value"]
+    assert round(8 * 8192 * oracle.kv_bytes_per_token(cfg) / 1e9, 2) == gold["kv_fleet_8x8192_gb"]["value"]
+
+
+def test_printed_sizes_reject_plausible_mistakes():
+    """The size pins fail for the nearby wrong schedules (a guard on the pins themselves)."""
+    gold = json.load(open(os.path.join(GOLD, "e2b_printed_sizes.json")))
+    cfg = synth.get_config("e2b")
+    for k, v in (("mlp_shared", 6144), ("num_kv_shared_layers", 0), ("full_every", 4),
+                 ("head_dim_full", 256)):
+        bad = dict(cfg, **{k: v})
+        c = oracle.param_counts(bad)
+        ok = (c["n_linears"] == gold["packed_int4_linears"]["value"]
+              and round(c["w4a16_bytes"] / 1e9, 3) == gold["w4a16_weight_gb"]["value"]
+              and oracle.kv_bytes_per_token(bad) == gold["kv_bytes_per_token"]["value"])
+        assert not ok, k
