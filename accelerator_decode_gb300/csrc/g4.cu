@@ -1,0 +1,999 @@
+// libg4: C ABI of the GB300 greedy decode step (see include/g4.h).
+//
+// One decode step, for n sequences (launch order; every kernel reads only what earlier
+// launches on the stream wrote):
+//   embed            x0 = E[t] sqrt(H); tok = T_ple[t] sqrt(P)
+//   gemv pmp         pr = W_pmp x0
+//   ple_combine      ple_l = (RMSNorm(pr_l H^-1/2) + tok_l) / sqrt 2
+//   per layer l:
+//     gemv qkv       prologue x = (x + RMSNorm(r_ple)) lambda_{l-1}; h = RMSNorm(x); y = W_qkv h
+//     attention      q/k norm + RoPE, K/V write (owning layers), flash-decode over cache[src]
+//     gemv o         r_attn = W_o o
+//     gemv gate/up   prologue x += RMSNorm(r_attn); m = RMSNorm(x); act = gelu(W_g m) * (W_u m)
+//     gemv down      r_mlp = W_d act
+//     gemv ple_gate  prologue x += RMSNorm(r_mlp); g = gelu(W_pg x) * ple_l
+//     gemv ple_proj  r_ple = W_pp g
+//   gemv lm_head     prologue x = (x + RMSNorm(r_ple)) lambda; y = RMSNorm(x); logits = E y,
+//                    block argmax + last-block reduction -> next ids
+// Decode steps are captured into a CUDA graph per (n, pointer set) and replayed.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "attn.cuh"
+#include "common.cuh"
+#include "gemv.cuh"
+#include "misc.cuh"
+
+using namespace g4;
+
+namespace {
+
+thread_local std::string g_last_cuda;
+
+bool cuda_ok(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return true;
+  char buf[512];
+  snprintf(buf, sizeof buf, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  g_last_cuda = buf;
+  return false;
+}
+#define CK(call)                                           \
+  do {                                                     \
+    if (!cuda_ok((call), #call)) return G4_ERR_CUDA;       \
+  } while (0)
+
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+struct Seg {
+  const void* w;
+  const void* s;
+  int rows;
+};
+
+// A projection in the tiled layout with its launch plan.
+struct Lin {
+  int fmt = 0, N = 0, K = 0, n_rb = 0, S = 0, tiles = 0, R = 1;
+  int n_valid = 0;  // outputs
+  int sg_per_cta = 1, ksplit = 1;
+  uint4* qw = nullptr;
+  uint4* sc = nullptr;
+  size_t bytes = 0;
+};
+
+struct Layer {
+  int full = 0, d = 0, F = 0, own = 0, src = 0, kv = -1;
+  Lin qkv, o, gu, down, pg, pp;
+  const __nv_bfloat16 *in_norm, *post_attn_norm, *pre_ffw_norm, *post_ffw_norm, *post_ple_norm, *q_norm, *k_norm;
+  float lambda = 1.f;
+  float scale = 1.f;
+  int attn_hpc = 1;
+};
+
+struct GraphKey {
+  int n;
+  const void *slots, *tokens, *pos, *next, *logits, *trace;
+  bool operator<(const GraphKey& o) const {
+    return std::tie(n, slots, tokens, pos, next, logits, trace) <
+           std::tie(o.n, o.slots, o.tokens, o.pos, o.next, o.logits, o.trace);
+  }
+};
+
+}  // namespace
+
+struct g4_handle {
+  g4_config cfg{};
+  int device = 0, sms = 0;
+  std::vector<void*> allocs;
+  size_t bytes = 0;
+  std::vector<Layer> layers;
+  Lin pmp, lm;
+  const __nv_bfloat16 *embed = nullptr, *ple_table = nullptr, *g_ppn = nullptr, *g_final = nullptr;
+  std::vector<__nv_bfloat16*> kc, vc;  // per owning layer
+  float *cos_t[2] = {nullptr, nullptr}, *sin_t[2] = {nullptr, nullptr};
+  // activations
+  float *x0 = nullptr, *xb[2] = {nullptr, nullptr}, *tok = nullptr, *pr = nullptr, *ple = nullptr;
+  float *qkv = nullptr, *attn = nullptr, *r_attn = nullptr, *act = nullptr, *r_mlp = nullptr, *pg = nullptr,
+        *r_ple = nullptr;
+  // scratch
+  float* gemv_part = nullptr;
+  unsigned* gemv_cnt = nullptr;
+  size_t gemv_part_floats = 0, gemv_cnt_n = 0;
+  float* am_val = nullptr;
+  int* am_idx = nullptr;
+  size_t am_n = 0;
+  float *attn_ml = nullptr, *attn_o = nullptr;
+  unsigned* attn_cnt = nullptr;
+  size_t attn_ml_n = 0, attn_o_n = 0;
+  int* err = nullptr;
+  // prefill staging
+  int* pf_buf = nullptr;
+  size_t pf_cap = 0;
+  int* step_next = nullptr;
+  float* step_logits = nullptr;
+  // trace
+  float* trace = nullptr;
+  int trace_stride = 0;
+  // graphs
+  std::map<GraphKey, cudaGraphExec_t> graphs;
+};
+
+namespace {
+
+template <class T>
+g4_status dalloc(g4_handle* h, T** p, size_t count) {
+  void* q = nullptr;
+  const size_t nbytes = std::max<size_t>(count, 1) * sizeof(T);
+  cudaError_t e = cudaMalloc(&q, nbytes);
+  if (e != cudaSuccess) {
+    cuda_ok(e, "cudaMalloc");
+    return e == cudaErrorMemoryAllocation ? G4_ERR_OOM : G4_ERR_CUDA;
+  }
+  h->allocs.push_back(q);
+  h->bytes += nbytes;
+  *p = reinterpret_cast<T*>(q);
+  return G4_OK;
+}
+#define TRY(x)                          \
+  do {                                  \
+    g4_status s_ = (x);                 \
+    if (s_ != G4_OK) return s_;         \
+  } while (0)
+
+int sgk(int fmt) { return fmt == G4_W4A16 ? Fmt<FMT_W4A16>::SGK : Fmt<FMT_BF16>::SGK; }
+
+// Choose the per-CTA K chunk: enough CTAs to cover the SMs a few times, fewer, fatter CTAs
+// for very tall matrices.
+void plan_lin(Lin& L, int sms, bool whole_k) {
+  const int n_rg = L.n_rb / L.R;
+  int spw = 1;
+  auto sgpc = [&](int s) { return std::min(L.S, kGemvWarps * s); };
+  while (sgpc(spw) < L.S && (whole_k || (long)n_rg * cdiv(L.S, sgpc(spw)) > 3L * sms)) spw *= 2;
+  L.sg_per_cta = sgpc(spw);
+  L.ksplit = cdiv(L.S, L.sg_per_cta);
+}
+
+// Build one tiled projection from row segments (each a multiple of 32 rows, except the
+// last block of a single-segment matrix).  interleave: segments {gate, up} alternate
+// 32-row blocks (R = 2) for the GeGLU epilogue.
+g4_status build_lin(g4_handle* h, int fmt, int K, const std::vector<Seg>& segs, bool interleave, Lin* out,
+                    cudaStream_t st, std::vector<RbSrc>& staging_keepalive) {
+  Lin L;
+  L.fmt = fmt;
+  L.K = K;
+  L.R = interleave ? 2 : 1;
+  std::vector<RbSrc> rbs;
+  const size_t rowbytes_w = fmt == G4_W4A16 ? (size_t)K / 2 : (size_t)K * 2;
+  const size_t rowbytes_s = (size_t)K / 32 * 2;
+  auto seg_blocks = [&](const Seg& s, std::vector<RbSrc>& v) {
+    for (int r0 = 0; r0 < s.rows; r0 += 32) {
+      RbSrc b;
+      b.w = static_cast<const char*>(s.w) + r0 * rowbytes_w;
+      b.s = s.s ? static_cast<const char*>(s.s) + r0 * rowbytes_s : nullptr;
+      b.rows = std::min(32, s.rows - r0);
+      b.pad = 0;
+      v.push_back(b);
+    }
+  };
+  if (interleave) {
+    std::vector<RbSrc> g, u;
+    seg_blocks(segs[0], g);
+    seg_blocks(segs[1], u);
+    for (size_t i = 0; i < g.size(); ++i) { rbs.push_back(g[i]); rbs.push_back(u[i]); }
+    L.n_valid = segs[0].rows;
+  } else {
+    int n = 0;
+    for (const Seg& s : segs) { seg_blocks(s, rbs); n += s.rows; }
+    L.n_valid = n;
+  }
+  while (rbs.size() % L.R) rbs.push_back(RbSrc{nullptr, nullptr, 0, 0});
+  L.n_rb = (int)rbs.size();
+  L.N = L.n_rb * 32;
+  L.S = cdiv(K, sgk(fmt));
+  L.tiles = 8 * L.S;
+  TRY(dalloc(h, &L.qw, (size_t)L.n_rb * L.tiles * 32));
+  L.bytes = (size_t)L.n_rb * L.tiles * 32 * 16;
+  if (fmt == G4_W4A16) {
+    TRY(dalloc(h, &L.sc, (size_t)L.n_rb * L.S * 32));
+    L.bytes += (size_t)L.n_rb * L.S * 32 * 16;
+  }
+  RbSrc* d_rbs = nullptr;
+  CK(cudaMalloc(&d_rbs, rbs.size() * sizeof(RbSrc)));
+  cudaError_t e = cudaMemcpy(d_rbs, rbs.data(), rbs.size() * sizeof(RbSrc), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) {
+    const int blocks = 4 * h->sms;
+    if (fmt == G4_W4A16) {
+      repack_int4_kernel<<<blocks, 256, 0, st>>>(d_rbs, L.n_rb, K, L.tiles, L.qw);
+      repack_scales_kernel<<<blocks, 256, 0, st>>>(d_rbs, L.n_rb, K, L.S, L.sc);
+    } else {
+      repack_bf16_kernel<<<blocks, 256, 0, st>>>(d_rbs, L.n_rb, K, L.tiles, L.qw);
+    }
+    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  }
+  cudaFree(d_rbs);
+  CK(e);
+  (void)staging_keepalive;
+  *out = L;
+  return G4_OK;
+}
+
+// ---------------------------------------------------------------------------- GEMV launch
+struct GemvIO {
+  int pro = PRO_PLAIN;
+  const float* x_in = nullptr;
+  int x_stride = 0;
+  const float* r_in = nullptr;
+  int r_stride = 0;
+  const __nv_bfloat16* g_r = nullptr;
+  float lambda = 1.f;
+  const __nv_bfloat16* g_a = nullptr;
+  float* x_out = nullptr;
+  int norm_n = 0;
+  float* y = nullptr;
+  int y_stride = 0;
+  const float* ple = nullptr;
+  int ple_stride = 0;
+  float* logits = nullptr;
+  int logits_stride = 0;
+  int* next_ids = nullptr;
+};
+
+struct Scratch {
+  float* part;
+  unsigned* cnt;
+  float* am_val;
+  int* am_idx;
+};
+
+template <int FMT, int R, int EPI, int NB>
+void launch_nb(const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
+  auto k = gemv_kernel<FMT, R, NB, EPI>;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k<<<grid, kGemvThreads, smem, st>>>(a);
+}
+
+template <int FMT, int R, int EPI>
+void launch_fmt(const GemvArgs& a, int nb, int grid, int sg_per_cta, cudaStream_t st) {
+  if (nb == 1) launch_nb<FMT, R, EPI, 1>(a, grid, gemv_smem_bytes<FMT, R, 1>(sg_per_cta), st);
+  else if (nb == 2) launch_nb<FMT, R, EPI, 2>(a, grid, gemv_smem_bytes<FMT, R, 2>(sg_per_cta), st);
+  else launch_nb<FMT, R, EPI, 4>(a, grid, gemv_smem_bytes<FMT, R, 4>(sg_per_cta), st);
+}
+
+// y = W x for n rows, in chunks of kMaxNB rows.
+void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const Scratch& s, cudaStream_t st) {
+  for (int b0 = 0; b0 < n; b0 += kMaxNB) {
+    const int nb = std::min(kMaxNB, n - b0);
+    GemvArgs a{};
+    a.qw = L.qw;
+    a.sc = L.sc;
+    a.n_rb = L.n_rb;
+    a.n_valid = L.n_valid;
+    a.K = L.K;
+    a.S = L.S;
+    a.tiles = L.tiles;
+    a.nb = nb;
+    a.ksplit = L.ksplit;
+    a.sg_per_cta = L.sg_per_cta;
+    a.pro = io.pro;
+    a.x_in = io.x_in + (size_t)b0 * io.x_stride;
+    a.x_stride = io.x_stride;
+    a.r_in = io.r_in ? io.r_in + (size_t)b0 * io.r_stride : nullptr;
+    a.r_stride = io.r_stride;
+    a.g_r = io.g_r;
+    a.lambda = io.lambda;
+    a.g_a = io.g_a;
+    a.x_out = io.x_out ? io.x_out + (size_t)b0 * io.x_stride : nullptr;
+    a.eps = eps;
+    a.norm_n = io.norm_n;
+    a.y = io.y ? io.y + (size_t)b0 * io.y_stride : nullptr;
+    a.y_stride = io.y_stride;
+    a.ple = io.ple ? io.ple + (size_t)b0 * io.ple_stride : nullptr;
+    a.ple_stride = io.ple_stride;
+    a.logits = io.logits ? io.logits + (size_t)b0 * io.logits_stride : nullptr;
+    a.logits_stride = io.logits_stride;
+    a.am_val = s.am_val;
+    a.am_idx = s.am_idx;
+    a.next_ids = io.next_ids ? io.next_ids + b0 : nullptr;
+    a.part = s.part;
+    a.counters = s.cnt;
+    const int grid = (L.n_rb / L.R) * L.ksplit;
+    const bool w4 = L.fmt == G4_W4A16;
+    switch (epi) {
+      case EPI_STORE:
+        if (w4) launch_fmt<FMT_W4A16, 1, EPI_STORE>(a, nb, grid, L.sg_per_cta, st);
+        else launch_fmt<FMT_BF16, 1, EPI_STORE>(a, nb, grid, L.sg_per_cta, st);
+        break;
+      case EPI_GEGLU:
+        if (w4) launch_fmt<FMT_W4A16, 2, EPI_GEGLU>(a, nb, grid, L.sg_per_cta, st);
+        else launch_fmt<FMT_BF16, 2, EPI_GEGLU>(a, nb, grid, L.sg_per_cta, st);
+        break;
+      case EPI_PLE:
+        if (w4) launch_fmt<FMT_W4A16, 1, EPI_PLE>(a, nb, grid, L.sg_per_cta, st);
+        else launch_fmt<FMT_BF16, 1, EPI_PLE>(a, nb, grid, L.sg_per_cta, st);
+        break;
+      case EPI_ARGMAX:
+        launch_fmt<FMT_BF16, 1, EPI_ARGMAX>(a, nb, grid, L.sg_per_cta, st);
+        break;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------- attention launch
+template <int D, int HPC>
+void launch_attn(const AttnArgs& a, int nb, cudaStream_t st) {
+  dim3 grid(a.nsplit, a.nq / HPC, nb);
+  attn_kernel<D, HPC><<<grid, kAttnThreads, 0, st>>>(a);
+}
+template <int D>
+void launch_attn_d(const AttnArgs& a, int hpc, int nb, cudaStream_t st) {
+  switch (hpc) {
+    case 1: launch_attn<D, 1>(a, nb, st); break;
+    case 2: launch_attn<D, 2>(a, nb, st); break;
+    case 4: launch_attn<D, 4>(a, nb, st); break;
+    default: launch_attn<D, 8>(a, nb, st); break;
+  }
+}
+
+int attn_hpc(int nq, int nb) {
+  if (nb <= 2) return 1;
+  int h = 8;
+  while (h > 1 && nq % h) h >>= 1;
+  return h;
+}
+int attn_nsplit(int sms, int nq, int hpc, int nb, int max_keys) {
+  const int n_hg = nq / hpc;
+  int ns = cdiv(2 * sms, nb * n_hg);
+  ns = std::min(ns, std::max(1, cdiv(max_keys, kAttnTile)));
+  return std::max(1, std::min(ns, 64));
+}
+
+// ------------------------------------------------------------------------------- the step
+g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens, const int* d_idx,
+                   const int* d_pos, int* d_next, float* d_logits) {
+  const g4_config& c = h->cfg;
+  const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
+  const float eps = c.rms_eps;
+  Scratch s{h->gemv_part, h->gemv_cnt, h->am_val, h->am_idx};
+
+  EmbedArgs ea{d_tokens, d_idx, h->embed, h->ple_table, c.vocab, H, LP,
+               (float)std::sqrt((double)H), (float)std::sqrt((double)P), h->x0, h->tok, h->err};
+  embed_kernel<<<n, 256, 0, st>>>(ea);
+  {
+    GemvIO io;
+    io.pro = PRO_PLAIN;
+    io.x_in = h->x0;
+    io.x_stride = H;
+    io.y = h->pr;
+    io.y_stride = LP;
+    run_gemv(h->pmp, EPI_STORE, io, n, eps, s, st);
+  }
+  ple_combine_kernel<<<dim3(L, n), std::min(256, std::max(32, P)), 0, st>>>(
+      h->pr, h->tok, h->g_ppn, L, P, (float)(1.0 / std::sqrt((double)H)), (float)(1.0 / std::sqrt(2.0)), eps, h->ple);
+
+  float* cur = h->x0;
+  auto next_x = [&]() { return cur == h->xb[0] ? h->xb[1] : h->xb[0]; };
+  const int ts = h->trace_stride;
+  for (int l = 0; l < L; ++l) {
+    Layer& Y = h->layers[l];
+    const int nqd = c.num_q_heads * Y.d;
+    {  // QKV
+      GemvIO io;
+      io.x_in = cur;
+      io.x_stride = H;
+      io.norm_n = H;
+      io.g_a = Y.in_norm;
+      if (l == 0) {
+        io.pro = PRO_NORM;
+      } else {
+        const Layer& Pv = h->layers[l - 1];
+        io.pro = PRO_RESID;
+        io.r_in = h->r_ple;
+        io.r_stride = H;
+        io.g_r = Pv.post_ple_norm;
+        io.lambda = Pv.lambda;
+        io.x_out = next_x();
+      }
+      io.y = h->qkv;
+      io.y_stride = Y.qkv.n_valid;
+      run_gemv(Y.qkv, EPI_STORE, io, n, eps, s, st);
+      if (l > 0) {
+        cur = io.x_out;
+        if (h->trace)
+          for (int i = 0; i < n; ++i)
+            cudaMemcpyAsync(h->trace + ((size_t)((l - 1) * 2 + 1) * c.max_batch + i) * ts, cur + (size_t)i * H,
+                            H * sizeof(float), cudaMemcpyDeviceToDevice, st);
+      }
+    }
+    {  // attention
+      const Layer& Src = h->layers[Y.src];
+      AttnArgs a{};
+      a.qkv = h->qkv;
+      a.qkv_stride = Y.qkv.n_valid;
+      a.nq = c.num_q_heads;
+      a.g_q = Y.q_norm;
+      a.g_k = Y.k_norm;
+      a.eps = eps;
+      a.scale = Y.scale;
+      a.window = Y.full ? 0 : c.sliding_window;
+      a.own = Y.own;
+      a.kc = h->kc[Src.kv];
+      a.vc = h->vc[Src.kv];
+      a.t_max = c.max_context;
+      a.max_batch = c.max_batch;
+      a.rope_cos = h->cos_t[Y.full];
+      a.rope_sin = h->sin_t[Y.full];
+      a.slots = d_slots;
+      a.positions = d_pos;
+      a.out = h->attn;
+      a.out_stride = nqd;
+      const int hpc = attn_hpc(c.num_q_heads, n);
+      a.nsplit = attn_nsplit(h->sms, c.num_q_heads, hpc, n, Y.full ? c.max_context : std::min(c.sliding_window, c.max_context));
+      a.ws_ml = h->attn_ml;
+      a.ws_o = h->attn_o;
+      a.counters = h->attn_cnt;
+      a.err = h->err;
+      switch (Y.d) {
+        case 64: launch_attn_d<64>(a, hpc, n, st); break;
+        case 128: launch_attn_d<128>(a, hpc, n, st); break;
+        case 256: launch_attn_d<256>(a, hpc, n, st); break;
+        default: launch_attn_d<512>(a, hpc, n, st); break;
+      }
+      if (h->trace)
+        for (int i = 0; i < n; ++i)
+          cudaMemcpyAsync(h->trace + ((size_t)(l * 2) * c.max_batch + i) * ts, h->attn + (size_t)i * nqd,
+                          nqd * sizeof(float), cudaMemcpyDeviceToDevice, st);
+    }
+    {  // O
+      GemvIO io;
+      io.pro = PRO_PLAIN;
+      io.x_in = h->attn;
+      io.x_stride = nqd;
+      io.y = h->r_attn;
+      io.y_stride = H;
+      run_gemv(Y.o, EPI_STORE, io, n, eps, s, st);
+    }
+    {  // gate/up
+      GemvIO io;
+      io.pro = PRO_RESID;
+      io.x_in = cur;
+      io.x_stride = H;
+      io.norm_n = H;
+      io.r_in = h->r_attn;
+      io.r_stride = H;
+      io.g_r = Y.post_attn_norm;
+      io.lambda = 1.f;
+      io.g_a = Y.pre_ffw_norm;
+      io.x_out = next_x();
+      io.y = h->act;
+      io.y_stride = Y.F;
+      run_gemv(Y.gu, EPI_GEGLU, io, n, eps, s, st);
+      cur = io.x_out;
+    }
+    {  // down
+      GemvIO io;
+      io.pro = PRO_PLAIN;
+      io.x_in = h->act;
+      io.x_stride = Y.F;
+      io.y = h->r_mlp;
+      io.y_stride = H;
+      run_gemv(Y.down, EPI_STORE, io, n, eps, s, st);
+    }
+    {  // PLE gate
+      GemvIO io;
+      io.pro = PRO_RESID;
+      io.x_in = cur;
+      io.x_stride = H;
+      io.norm_n = H;
+      io.r_in = h->r_mlp;
+      io.r_stride = H;
+      io.g_r = Y.post_ffw_norm;
+      io.lambda = 1.f;
+      io.g_a = nullptr;
+      io.x_out = next_x();
+      io.y = h->pg;
+      io.y_stride = P;
+      io.ple = h->ple + (size_t)l * P;
+      io.ple_stride = LP;
+      run_gemv(Y.pg, EPI_PLE, io, n, eps, s, st);
+      cur = io.x_out;
+    }
+    {  // PLE proj
+      GemvIO io;
+      io.pro = PRO_PLAIN;
+      io.x_in = h->pg;
+      io.x_stride = P;
+      io.y = h->r_ple;
+      io.y_stride = H;
+      run_gemv(Y.pp, EPI_STORE, io, n, eps, s, st);
+    }
+  }
+  {  // final norm, lm_head, argmax
+    const Layer& Pv = h->layers[L - 1];
+    GemvIO io;
+    io.pro = PRO_RESID;
+    io.x_in = cur;
+    io.x_stride = H;
+    io.norm_n = H;
+    io.r_in = h->r_ple;
+    io.r_stride = H;
+    io.g_r = Pv.post_ple_norm;
+    io.lambda = Pv.lambda;
+    io.g_a = h->g_final;
+    io.x_out = next_x();
+    io.logits = d_logits;
+    io.logits_stride = c.vocab;
+    io.next_ids = d_next;
+    run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, st);
+    if (h->trace)
+      for (int i = 0; i < n; ++i)
+        cudaMemcpyAsync(h->trace + ((size_t)((L - 1) * 2 + 1) * c.max_batch + i) * ts, io.x_out + (size_t)i * H,
+                        H * sizeof(float), cudaMemcpyDeviceToDevice, st);
+  }
+  CK(cudaGetLastError());
+  return G4_OK;
+}
+
+bool is_pow2_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
+
+g4_status validate(const g4_config* c) {
+  if (!c) return G4_ERR_INVALID_ARG;
+  if (c->num_layers < 1 || c->num_kv_shared_layers < 0 || c->num_kv_shared_layers >= c->num_layers)
+    return G4_ERR_INVALID_ARG;
+  if (c->hidden < 32 || c->num_q_heads < 1 || c->vocab < 1 || c->ple_dim < 1 || c->mlp < 32 || c->mlp_shared < 32)
+    return G4_ERR_INVALID_ARG;
+  if (c->max_batch < 1 || c->max_context < 1 || c->full_every < 1 || c->sliding_window < 1) return G4_ERR_INVALID_ARG;
+  if (c->weight_format != G4_BF16 && c->weight_format != G4_W4A16) return G4_ERR_INVALID_ARG;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta_sliding > 0.f) || !(c->rope_theta_full > 0.f)) return G4_ERR_INVALID_ARG;
+  if (c->num_kv_heads != 1 || c->group_size != 32) return G4_ERR_UNSUPPORTED;
+  if (!is_pow2_dim(c->head_dim_sliding) || !is_pow2_dim(c->head_dim_full)) return G4_ERR_UNSUPPORTED;
+  if (c->hidden % 32 || c->mlp % 32 || c->mlp_shared % 32 || c->ple_dim % 32) return G4_ERR_UNSUPPORTED;
+  if (c->max_batch > 64 || c->ple_dim > 1024) return G4_ERR_UNSUPPORTED;
+  return G4_OK;
+}
+
+g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, cudaStream_t st) {
+  const g4_config& c = *cfg;
+  const int L = c.num_layers, H = c.hidden, P = c.ple_dim, nq = c.num_q_heads;
+  const int first = L - c.num_kv_shared_layers;
+  const int fmt = c.weight_format;
+  std::vector<RbSrc> keep;
+  h->embed = static_cast<const __nv_bfloat16*>(w->embed);
+  h->ple_table = static_cast<const __nv_bfloat16*>(w->ple_table);
+  h->g_ppn = static_cast<const __nv_bfloat16*>(w->ple_proj_norm);
+  h->g_final = static_cast<const __nv_bfloat16*>(w->final_norm);
+  if (!h->embed || !h->ple_table || !h->g_ppn || !h->g_final || !w->layers || !w->ple_model_proj.w)
+    return G4_ERR_INVALID_ARG;
+  if (fmt == G4_W4A16 && !w->ple_model_proj.scales) return G4_ERR_INVALID_ARG;
+
+  // layer schedule: type, share source, ownership ("One TPU chip, eight agents", The engine)
+  std::vector<int> full(L), src(L);
+  int last_of[2] = {-1, -1};
+  for (int l = 0; l < L; ++l) full[l] = (l % c.full_every) == c.full_every - 1;
+  for (int l = 0; l < first; ++l) last_of[full[l]] = l;
+  for (int l = 0; l < L; ++l) src[l] = (l < first || last_of[full[l]] < 0) ? l : last_of[full[l]];
+
+  h->layers.resize(L);
+  int n_own = 0;
+  for (int l = 0; l < L; ++l) {
+    Layer& Y = h->layers[l];
+    const g4_layer_weights& lw = w->layers[l];
+    Y.full = full[l];
+    Y.d = Y.full ? c.head_dim_full : c.head_dim_sliding;
+    Y.F = l >= first ? c.mlp_shared : c.mlp;
+    Y.src = src[l];
+    Y.own = src[l] == l;
+    Y.kv = Y.own ? n_own++ : -1;
+    const float sc = Y.full ? c.attn_scale_full : c.attn_scale_sliding;
+    Y.scale = sc != 0.f ? sc : (float)(1.0 / std::sqrt((double)Y.d));
+    Y.lambda = lw.layer_scale;
+    Y.in_norm = (const __nv_bfloat16*)lw.in_norm;
+    Y.post_attn_norm = (const __nv_bfloat16*)lw.post_attn_norm;
+    Y.pre_ffw_norm = (const __nv_bfloat16*)lw.pre_ffw_norm;
+    Y.post_ffw_norm = (const __nv_bfloat16*)lw.post_ffw_norm;
+    Y.post_ple_norm = (const __nv_bfloat16*)lw.post_ple_norm;
+    Y.q_norm = (const __nv_bfloat16*)lw.q_norm;
+    Y.k_norm = (const __nv_bfloat16*)lw.k_norm;
+    if (!Y.in_norm || !Y.post_attn_norm || !Y.pre_ffw_norm || !Y.post_ffw_norm || !Y.post_ple_norm || !Y.q_norm)
+      return G4_ERR_INVALID_ARG;
+    const g4_linear* need[] = {&lw.q, &lw.o, &lw.gate, &lw.up, &lw.down, &lw.ple_gate, &lw.ple_proj};
+    for (const g4_linear* p : need)
+      if (!p->w || (fmt == G4_W4A16 && !p->scales)) return G4_ERR_INVALID_ARG;
+    if (Y.own && (!lw.k.w || !lw.v.w || !Y.k_norm || (fmt == G4_W4A16 && (!lw.k.scales || !lw.v.scales))))
+      return G4_ERR_INVALID_ARG;
+    const int nqd = nq * Y.d;
+    std::vector<Seg> qkv = {{lw.q.w, lw.q.scales, nqd}};
+    if (Y.own) {
+      qkv.push_back({lw.k.w, lw.k.scales, Y.d});
+      qkv.push_back({lw.v.w, lw.v.scales, Y.d});
+    }
+    TRY(build_lin(h, fmt, H, qkv, false, &Y.qkv, st, keep));
+    TRY(build_lin(h, fmt, nqd, {{lw.o.w, lw.o.scales, H}}, false, &Y.o, st, keep));
+    TRY(build_lin(h, fmt, H, {{lw.gate.w, lw.gate.scales, Y.F}, {lw.up.w, lw.up.scales, Y.F}}, true, &Y.gu, st, keep));
+    TRY(build_lin(h, fmt, Y.F, {{lw.down.w, lw.down.scales, H}}, false, &Y.down, st, keep));
+    TRY(build_lin(h, fmt, H, {{lw.ple_gate.w, lw.ple_gate.scales, P}}, false, &Y.pg, st, keep));
+    TRY(build_lin(h, fmt, P, {{lw.ple_proj.w, lw.ple_proj.scales, H}}, false, &Y.pp, st, keep));
+    for (Lin* Ln : {&Y.qkv, &Y.o, &Y.gu, &Y.down, &Y.pg, &Y.pp}) plan_lin(*Ln, h->sms, false);
+  }
+  TRY(build_lin(h, fmt, H, {{w->ple_model_proj.w, w->ple_model_proj.scales, L * P}}, false, &h->pmp, st, keep));
+  plan_lin(h->pmp, h->sms, false);
+  TRY(build_lin(h, G4_BF16, H, {{w->embed, nullptr, c.vocab}}, false, &h->lm, st, keep));
+  plan_lin(h->lm, h->sms, true);
+
+  // KV cache: owning layers only; [max_batch][max_context][d] bf16 each for K and V.
+  h->kc.resize(n_own);
+  h->vc.resize(n_own);
+  for (int l = 0; l < L; ++l) {
+    const Layer& Y = h->layers[l];
+    if (!Y.own) continue;
+    const size_t n = (size_t)c.max_batch * c.max_context * Y.d;
+    TRY(dalloc(h, &h->kc[Y.kv], n));
+    TRY(dalloc(h, &h->vc[Y.kv], n));
+    CK(cudaMemsetAsync(h->kc[Y.kv], 0, n * 2, st));
+    CK(cudaMemsetAsync(h->vc[Y.kv], 0, n * 2, st));
+  }
+  // RoPE tables (fp64 angles, rounded to fp32)
+  for (int t = 0; t < 2; ++t) {
+    const int d = t ? c.head_dim_full : c.head_dim_sliding;
+    const double theta = t ? c.rope_theta_full : c.rope_theta_sliding;
+    std::vector<float> cs((size_t)c.max_context * d / 2), sn(cs.size());
+    for (int i = 0; i < d / 2; ++i) {
+      const double inv = std::pow(theta, -2.0 * i / d);
+      for (int p = 0; p < c.max_context; ++p) {
+        const double ang = (double)p * inv;
+        cs[(size_t)p * (d / 2) + i] = (float)std::cos(ang);
+        sn[(size_t)p * (d / 2) + i] = (float)std::sin(ang);
+      }
+    }
+    TRY(dalloc(h, &h->cos_t[t], cs.size()));
+    TRY(dalloc(h, &h->sin_t[t], sn.size()));
+    CK(cudaMemcpy(h->cos_t[t], cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(h->sin_t[t], sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
+  }
+  // activations
+  const int B = c.max_batch;
+  const int dmax = std::max(c.head_dim_full, c.head_dim_sliding);
+  const int Fmax = std::max(c.mlp, c.mlp_shared);
+  TRY(dalloc(h, &h->x0, (size_t)B * H));
+  TRY(dalloc(h, &h->xb[0], (size_t)B * H));
+  TRY(dalloc(h, &h->xb[1], (size_t)B * H));
+  TRY(dalloc(h, &h->tok, (size_t)B * L * P));
+  TRY(dalloc(h, &h->pr, (size_t)B * L * P));
+  TRY(dalloc(h, &h->ple, (size_t)B * L * P));
+  TRY(dalloc(h, &h->qkv, (size_t)B * (nq + 2) * dmax));
+  TRY(dalloc(h, &h->attn, (size_t)B * nq * dmax));
+  TRY(dalloc(h, &h->r_attn, (size_t)B * H));
+  TRY(dalloc(h, &h->act, (size_t)B * Fmax));
+  TRY(dalloc(h, &h->r_mlp, (size_t)B * H));
+  TRY(dalloc(h, &h->pg, (size_t)B * P));
+  TRY(dalloc(h, &h->r_ple, (size_t)B * H));
+  // GEMV scratch: partials of the widest split, one counter per row group (+1 for argmax)
+  size_t part = 1, cnt = 1;
+  auto acc_lin = [&](const Lin& Ln) {
+    part = std::max(part, (size_t)Ln.ksplit * kMaxNB * Ln.n_rb * 32);
+    cnt = std::max(cnt, (size_t)(Ln.n_rb / Ln.R) * Ln.ksplit + 1);
+  };
+  for (const Layer& Y : h->layers)
+    for (const Lin* Ln : {&Y.qkv, &Y.o, &Y.gu, &Y.down, &Y.pg, &Y.pp}) acc_lin(*Ln);
+  acc_lin(h->pmp);
+  acc_lin(h->lm);
+  h->gemv_part_floats = part;
+  h->gemv_cnt_n = cnt;
+  TRY(dalloc(h, &h->gemv_part, part));
+  TRY(dalloc(h, &h->gemv_cnt, cnt));
+  CK(cudaMemsetAsync(h->gemv_cnt, 0, cnt * sizeof(unsigned), st));
+  h->am_n = (size_t)kMaxNB * (h->lm.n_rb / h->lm.R) * h->lm.ksplit;
+  TRY(dalloc(h, &h->am_val, h->am_n));
+  TRY(dalloc(h, &h->am_idx, h->am_n));
+  // attention scratch for the largest (nb * nsplit) over batch sizes
+  size_t ml = 1, ao = 1;
+  for (int nb = 1; nb <= B; ++nb) {
+    const int hpc = attn_hpc(nq, nb);
+    for (int t = 0; t < 2; ++t) {
+      const int d = t ? c.head_dim_full : c.head_dim_sliding;
+      const int keys = t ? c.max_context : std::min(c.sliding_window, c.max_context);
+      const int ns = attn_nsplit(h->sms, nq, hpc, nb, keys);
+      ml = std::max(ml, (size_t)nb * nq * ns * 2);
+      ao = std::max(ao, (size_t)nb * nq * ns * d);
+    }
+  }
+  h->attn_ml_n = ml;
+  h->attn_o_n = ao;
+  TRY(dalloc(h, &h->attn_ml, ml));
+  TRY(dalloc(h, &h->attn_o, ao));
+  TRY(dalloc(h, &h->attn_cnt, (size_t)B * nq));
+  CK(cudaMemsetAsync(h->attn_cnt, 0, (size_t)B * nq * sizeof(unsigned), st));
+  TRY(dalloc(h, &h->err, 1));
+  CK(cudaMemsetAsync(h->err, 0, sizeof(int), st));
+  TRY(dalloc(h, &h->step_next, B));
+  TRY(dalloc(h, &h->step_logits, (size_t)B * c.vocab));
+  CK(cudaStreamSynchronize(st));
+  return G4_OK;
+}
+
+void destroy(g4_handle* h) {
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+  for (void* p : h->allocs) cudaFree(p);
+  if (h->pf_buf) cudaFree(h->pf_buf);
+  delete h;
+}
+
+}  // namespace
+
+// =================================================================================== C ABI
+extern "C" {
+
+const char* g4_status_string(g4_status s) {
+  switch (s) {
+    case G4_OK: return "ok";
+    case G4_ERR_INVALID_ARG: return "invalid argument";
+    case G4_ERR_UNSUPPORTED: return "unsupported configuration";
+    case G4_ERR_OOM: return "out of device memory";
+    case G4_ERR_CUDA: return "CUDA error";
+    case G4_ERR_CONTEXT_OVERFLOW: return "context overflow";
+    case G4_ERR_TIMEOUT: return "device wait timed out";
+    case G4_ERR_DEVICE_CHECK: return "device-side argument check failed";
+  }
+  return "unknown status";
+}
+
+const char* g4_last_cuda_error(void) { return g_last_cuda.c_str(); }
+
+g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device, g4_handle** out) {
+  if (!out) return G4_ERR_INVALID_ARG;
+  *out = nullptr;
+  g4_status v = validate(cfg);
+  if (v != G4_OK) return v;
+  if (!weights) return G4_ERR_INVALID_ARG;
+  CK(cudaSetDevice(device));
+  g4_handle* h = new g4_handle();
+  h->cfg = *cfg;
+  h->device = device;
+  cudaError_t e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device);
+  if (!cuda_ok(e, "cudaDeviceGetAttribute")) { delete h; return G4_ERR_CUDA; }
+  cudaStream_t st = nullptr;
+  e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking);
+  if (!cuda_ok(e, "cudaStreamCreate")) { delete h; return G4_ERR_CUDA; }
+  g4_status s = create_impl(h, cfg, weights, st);
+  cudaStreamSynchronize(st);
+  cudaStreamDestroy(st);
+  if (s != G4_OK) { destroy(h); return s; }
+  *out = h;
+  return G4_OK;
+}
+
+void g4_free(g4_handle* h) {
+  if (h) destroy(h);
+}
+
+int64_t g4_device_bytes(const g4_handle* h) { return h ? (int64_t)h->bytes : 0; }
+
+g4_status g4_set_trace(g4_handle* h, float* d_trace, int64_t capacity_floats) {
+  if (!h) return G4_ERR_INVALID_ARG;
+  const g4_config& c = h->cfg;
+  const int stride = std::max(c.hidden, c.num_q_heads * std::max(c.head_dim_full, c.head_dim_sliding));
+  if (d_trace && capacity_floats < (int64_t)c.num_layers * 2 * c.max_batch * stride) return G4_ERR_INVALID_ARG;
+  h->trace = d_trace;
+  h->trace_stride = stride;
+  return G4_OK;
+}
+
+g4_status g4_decode_step(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_t* d_slots,
+                         const int32_t* d_tokens, const int32_t* d_positions, int32_t* d_next_ids, float* d_logits) {
+  if (!h || !d_slots || !d_tokens || !d_positions || !d_next_ids) return G4_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > h->cfg.max_batch) return G4_ERR_INVALID_ARG;
+  CK(cudaSetDevice(h->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (st == nullptr) {  // the legacy default stream cannot be captured: launch directly
+    return run_step(h, st, n_seq, d_slots, d_tokens, nullptr, d_positions, d_next_ids, d_logits);
+  }
+  GraphKey key{n_seq, d_slots, d_tokens, d_positions, d_next_ids, d_logits, h->trace};
+  auto it = h->graphs.find(key);
+  if (it == h->graphs.end()) {
+    if (h->graphs.size() >= 16) {
+      for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
+      h->graphs.clear();
+    }
+    CK(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+    g4_status s = run_step(h, st, n_seq, d_slots, d_tokens, nullptr, d_positions, d_next_ids, d_logits);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(st, &g);
+    if (s != G4_OK) { if (g) cudaGraphDestroy(g); return s; }
+    CK(e);
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    CK(e);
+    it = h->graphs.emplace(key, ex).first;
+  }
+  CK(cudaGraphLaunch(it->second, st));
+  return G4_OK;
+}
+
+g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_t* slots, const int32_t* offsets,
+                     const int32_t* start_pos, const int32_t* d_tokens, int32_t* d_next_ids, float* d_logits) {
+  if (!h || !slots || !offsets || !start_pos || !d_tokens || !d_next_ids) return G4_ERR_INVALID_ARG;
+  const g4_config& c = h->cfg;
+  if (n_seq < 1 || n_seq > c.max_batch) return G4_ERR_INVALID_ARG;
+  std::vector<int> len(n_seq), order(n_seq);
+  std::vector<char> used(c.max_batch, 0);
+  for (int i = 0; i < n_seq; ++i) {
+    len[i] = offsets[i + 1] - offsets[i];
+    if (len[i] < 1 || offsets[i] < 0) return G4_ERR_INVALID_ARG;
+    if (slots[i] < 0 || slots[i] >= c.max_batch || used[slots[i]]) return G4_ERR_INVALID_ARG;
+    used[slots[i]] = 1;
+    if (start_pos[i] < 0) return G4_ERR_INVALID_ARG;
+    if ((int64_t)start_pos[i] + len[i] > c.max_context) return G4_ERR_CONTEXT_OVERFLOW;
+    order[i] = i;
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return len[a] > len[b]; });
+  const int T = len[order[0]];
+  // per step t: slots, positions, token indices of the active prefix of `order`
+  std::vector<int> host((size_t)3 * T * n_seq, 0);
+  std::vector<int> n_act(T);
+  for (int t = 0; t < T; ++t) {
+    int n = 0;
+    for (int i = 0; i < n_seq; ++i) {
+      const int q = order[i];
+      if (len[q] <= t) break;
+      host[((size_t)0 * T + t) * n_seq + n] = slots[q];
+      host[((size_t)1 * T + t) * n_seq + n] = start_pos[q] + t;
+      host[((size_t)2 * T + t) * n_seq + n] = offsets[q] + t;
+      ++n;
+    }
+    n_act[t] = n;
+  }
+  CK(cudaSetDevice(h->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (h->pf_cap < host.size()) {
+    if (h->pf_buf) { CK(cudaStreamSynchronize(st)); cudaFree(h->pf_buf); h->pf_buf = nullptr; h->pf_cap = 0; }
+    CK(cudaMalloc(&h->pf_buf, host.size() * sizeof(int)));
+    h->pf_cap = host.size();
+  }
+  CK(cudaMemcpyAsync(h->pf_buf, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice, st));
+  CK(cudaStreamSynchronize(st));  // the host staging vector goes out of scope below
+  for (int t = 0; t < T; ++t) {
+    const int n = n_act[t];
+    const int* ds = h->pf_buf + ((size_t)0 * T + t) * n_seq;
+    const int* dp = h->pf_buf + ((size_t)1 * T + t) * n_seq;
+    const int* di = h->pf_buf + ((size_t)2 * T + t) * n_seq;
+    const int n_next = t + 1 < T ? n_act[t + 1] : 0;  // sequences finishing now: [n_next, n)
+    float* lg = (d_logits && n_next < n) ? h->step_logits : nullptr;
+    TRY(run_step(h, st, n, ds, d_tokens, di, dp, h->step_next, lg));
+    for (int i = n_next; i < n; ++i) {
+      const int q = order[i];
+      CK(cudaMemcpyAsync(d_next_ids + q, h->step_next + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
+      if (d_logits)
+        CK(cudaMemcpyAsync(d_logits + (size_t)q * c.vocab, h->step_logits + (size_t)i * c.vocab,
+                           (size_t)c.vocab * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    }
+  }
+  return G4_OK;
+}
+
+g4_status g4_get_device_error(g4_handle* h, g4_stream stream, int32_t* word_out) {
+  if (!h) return G4_ERR_INVALID_ARG;
+  CK(cudaSetDevice(h->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int w = 0;
+  CK(cudaMemcpyAsync(&w, h->err, sizeof(int), cudaMemcpyDeviceToHost, st));
+  CK(cudaMemsetAsync(h->err, 0, sizeof(int), st));
+  CK(cudaStreamSynchronize(st));
+  if (word_out) *word_out = w;
+  if (w & G4_DEV_TIMEOUT) return G4_ERR_TIMEOUT;
+  return w ? G4_ERR_DEVICE_CHECK : G4_OK;
+}
+
+// ------------------------------------------------------------------------ standalone ops
+struct g4_linear_op {
+  g4_handle h;  // owns the allocations
+  Lin lin;
+};
+
+g4_status g4_linear_create(int device, int32_t weight_format, int32_t n_out, int32_t n_in, const void* d_w,
+                           const void* d_scales, g4_linear_op** out) {
+  if (!out || !d_w || n_out < 1 || n_in < 32 || n_in % 32) return G4_ERR_INVALID_ARG;
+  if (weight_format != G4_BF16 && weight_format != G4_W4A16) return G4_ERR_INVALID_ARG;
+  if (weight_format == G4_W4A16 && !d_scales) return G4_ERR_INVALID_ARG;
+  *out = nullptr;
+  CK(cudaSetDevice(device));
+  g4_linear_op* op = new g4_linear_op();
+  op->h.device = device;
+  cudaDeviceGetAttribute(&op->h.sms, cudaDevAttrMultiProcessorCount, device);
+  cudaStream_t st = nullptr;
+  CK(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+  std::vector<RbSrc> keep;
+  g4_status s = build_lin(&op->h, weight_format, n_in, {{d_w, d_scales, n_out}}, false, &op->lin, st, keep);
+  if (s == G4_OK) {
+    plan_lin(op->lin, op->h.sms, false);
+    size_t part = (size_t)op->lin.ksplit * kMaxNB * op->lin.n_rb * 32;
+    size_t cnt = (size_t)op->lin.n_rb * op->lin.ksplit + 1;
+    s = dalloc(&op->h, &op->h.gemv_part, part);
+    if (s == G4_OK) s = dalloc(&op->h, &op->h.gemv_cnt, cnt);
+    if (s == G4_OK && !cuda_ok(cudaMemsetAsync(op->h.gemv_cnt, 0, cnt * 4, st), "memset")) s = G4_ERR_CUDA;
+  }
+  cudaStreamSynchronize(st);
+  cudaStreamDestroy(st);
+  if (s != G4_OK) {
+    for (void* p : op->h.allocs) cudaFree(p);
+    delete op;
+    return s;
+  }
+  *out = op;
+  return G4_OK;
+}
+
+g4_status g4_linear_forward(g4_linear_op* op, g4_stream stream, int32_t n_rows, const float* d_x, float* d_y) {
+  if (!op || !d_x || !d_y || n_rows < 1 || n_rows > 64) return G4_ERR_INVALID_ARG;
+  CK(cudaSetDevice(op->h.device));
+  GemvIO io;
+  io.pro = PRO_PLAIN;
+  io.x_in = d_x;
+  io.x_stride = op->lin.K;
+  io.y = d_y;
+  io.y_stride = op->lin.n_valid;
+  Scratch s{op->h.gemv_part, op->h.gemv_cnt, nullptr, nullptr};
+  run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, reinterpret_cast<cudaStream_t>(stream));
+  CK(cudaGetLastError());
+  return G4_OK;
+}
+
+void g4_linear_free(g4_linear_op* op) {
+  if (!op) return;
+  cudaSetDevice(op->h.device);
+  cudaDeviceSynchronize();
+  for (void* p : op->h.allocs) cudaFree(p);
+  delete op;
+}
+
+// Per-device scratch of the standalone argmax, grown on demand and kept until exit.
+namespace {
+struct ArgmaxScratch {
+  float* pv = nullptr;
+  int* pi = nullptr;
+  unsigned* cnt = nullptr;
+  size_t cap = 0;
+};
+std::mutex g_am_mu;
+std::map<int, ArgmaxScratch> g_am;
+}  // namespace
+
+g4_status g4_argmax_rows(int device, g4_stream stream, int32_t n_rows, int32_t n_cols, const float* d_logits,
+                         int32_t* d_ids) {
+  if (!d_logits || !d_ids || n_rows < 1 || n_rows > 64 || n_cols < 1) return G4_ERR_INVALID_ARG;
+  CK(cudaSetDevice(device));
+  const int chunk = 4096;
+  const int nchunk = cdiv(n_cols, chunk);
+  const size_t need = (size_t)n_rows * nchunk;
+  ArgmaxScratch* sc;
+  {
+    std::lock_guard<std::mutex> lk(g_am_mu);
+    sc = &g_am[device];
+    if (sc->cap < need) {
+      CK(cudaDeviceSynchronize());
+      cudaFree(sc->pv);
+      cudaFree(sc->pi);
+      cudaFree(sc->cnt);
+      *sc = ArgmaxScratch{};
+      CK(cudaMalloc(&sc->pv, need * sizeof(float)));
+      CK(cudaMalloc(&sc->pi, need * sizeof(int)));
+      CK(cudaMalloc(&sc->cnt, 64 * sizeof(unsigned)));
+      CK(cudaMemset(sc->cnt, 0, 64 * sizeof(unsigned)));
+      sc->cap = need;
+    }
+  }
+  argmax_rows_kernel<<<dim3(nchunk, n_rows), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      d_logits, n_cols, chunk, sc->pv, sc->pi, sc->cnt, d_ids);
+  CK(cudaGetLastError());
+  return G4_OK;
+}
+
+}  // extern "C"

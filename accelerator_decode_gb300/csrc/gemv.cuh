@@ -1,0 +1,393 @@
+// Weight-only projections for small batches (GEMV): y[b, n] = sum_k W[n, k] x[b, k].
+//
+// Device weight layout ("lane = row" tiles).  Rows are grouped in blocks of 32 (one per
+// lane); K is cut into 16-byte tiles per lane:
+//   W4A16: tile = one group of 32 int4 (16 B) of one row, offset-binary nibbles n = q + 8;
+//          word m (0..3) of a tile holds k = 8m..8m+7 of the group with k = 8m+2j at bits
+//          [4j, 4j+4) and k = 8m+2j+1 at bits [16+4j, 20+4j) (j = 0..3), so one mask+OR
+//          turns a nibble pair into a bf16x2 (128+n_even, 128+n_odd).
+//   bf16:  tile = 8 consecutive bf16 of one row.
+//   qw[(rb * tiles_per_row + t) * 32 + lane]: a warp reads 512 contiguous bytes per tile.
+//   W4A16 scales: sc[(rb * S + sg) * 32 + lane] = 8 bf16 (the 8 groups of supergroup sg).
+// A "supergroup" is 8 tiles of a row (256 k for W4A16, 64 k for bf16).
+//
+// Dequantisation is bf16(q * s): the nibble becomes an exact bf16 q by one subtraction
+// (bf16 128+n minus 136), then one bf16x2 multiply rounds q*s to nearest even, as
+// dequantising to bf16 does ("One TPU chip, eight agents", Two optimizations that didn't
+// work; "Gemma 4 E2B in Pure JAX on a Colab TPU", cell 1.2).  Accumulation is fp32 (packed
+// fp32x2 FMA) with fp32 activations.
+//
+// CTA = 4 warps on one row group (R row blocks); warps take different supergroups of the
+// CTA's K chunk; a K split over CTAs is reduced by the last CTA to finish, summing the
+// partials in split order (deterministic).  The prologue (norm / residual update) is
+// recomputed by every CTA from the full input vector; block 0 writes the new residual.
+#pragma once
+#include "common.cuh"
+
+namespace g4 {
+
+enum { FMT_BF16 = 0, FMT_W4A16 = 1 };
+enum { PRO_PLAIN = 0, PRO_NORM = 1, PRO_RESID = 2 };
+enum { EPI_STORE = 0, EPI_GEGLU = 1, EPI_PLE = 2, EPI_ARGMAX = 3 };
+
+constexpr int kGemvWarps = 4;
+constexpr int kGemvThreads = kGemvWarps * 32;
+constexpr int kMaxNB = 4;  // batch rows per GEMV launch
+
+struct GemvArgs {
+  const uint4* qw;
+  const uint4* sc;
+  int n_rb;       // 32-row blocks (padded)
+  int n_valid;    // valid outputs (rows; for GEGLU: output features)
+  int K;          // logical inner size (multiple of 32)
+  int S;          // supergroups along K
+  int tiles;      // tiles per row = 8 * S
+  int nb;         // batch rows in this launch (<= kMaxNB)
+  int ksplit;     // CTAs along K per row group
+  int sg_per_cta; // supergroups per CTA
+  // prologue
+  int pro;
+  const float* x_in;
+  int x_stride;
+  const float* r_in;
+  int r_stride;
+  const __nv_bfloat16* g_r;
+  float lambda;
+  const __nv_bfloat16* g_a;
+  float* x_out;
+  float eps;
+  int norm_n;     // length of the residual vector (== K for PRO_NORM / PRO_RESID)
+  // epilogue
+  float* y;
+  int y_stride;
+  const float* ple;
+  int ple_stride;
+  float* logits;   // EPI_ARGMAX: optional [nb, logits_stride]
+  int logits_stride;
+  float* am_val;   // EPI_ARGMAX partials [nb][gridDim.x]
+  int* am_idx;
+  int* next_ids;   // EPI_ARGMAX: [nb]
+  // split-K scratch
+  float* part;     // [ksplit][nb][n_rb * 32]
+  unsigned* counters;
+};
+
+template <int FMT>
+struct Fmt {
+  static constexpr int SGK = FMT == FMT_W4A16 ? 256 : 64;  // k per supergroup
+  static constexpr int TK = SGK / 8;                        // k per tile
+};
+
+// Accumulate one tile (one row, TK k values) into acc[b] for NB activation rows.
+template <int FMT, int NB>
+__device__ __forceinline__ void tile_fma(const uint4 wv, uint32_t s2, const float* xs, int xs_stride,
+                                         float2 (&acc)[NB]) {
+  const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+  if constexpr (FMT == FMT_W4A16) {
+    const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
+    const __nv_bfloat162 sc = as_bf162(s2);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float4 xa[NB], xb[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        xa[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride + 8 * m);
+        xb[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride + 8 * m + 4);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t u = ((w[m] >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+        __nv_bfloat162 q = __hsub2(as_bf162(u), bias);
+        uint32_t p = as_u32(__hmul2(q, sc));
+        float2 wf = make_float2(bf16_lo(p), bf16_hi(p));
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          float2 xv = j == 0 ? make_float2(xa[b].x, xa[b].y)
+                    : j == 1 ? make_float2(xa[b].z, xa[b].w)
+                    : j == 2 ? make_float2(xb[b].x, xb[b].y)
+                             : make_float2(xb[b].z, xb[b].w);
+          acc[b] = __ffma2_rn(wf, xv, acc[b]);
+        }
+      }
+    }
+  } else {
+    float4 xa[NB], xb[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      xa[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride);
+      xb[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride + 4);
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float2 wf = make_float2(bf16_lo(w[m]), bf16_hi(w[m]));
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float2 xv = m == 0 ? make_float2(xa[b].x, xa[b].y)
+                  : m == 1 ? make_float2(xa[b].z, xa[b].w)
+                  : m == 2 ? make_float2(xb[b].x, xb[b].y)
+                           : make_float2(xb[b].z, xb[b].w);
+        acc[b] = __ffma2_rn(wf, xv, acc[b]);
+      }
+    }
+  }
+}
+
+// Prologue: stage the activation chunk [k0, k1) of NB rows into smem (fp32), zero-padded.
+template <int NB>
+__device__ __forceinline__ void gemv_prologue(const GemvArgs& a, float* xs, int kc, int k0, int k1,
+                                              float* red) {
+  const int tid = threadIdx.x;
+  if (a.pro == PRO_PLAIN) {
+    for (int b = 0; b < NB; ++b) {
+      for (int k = k0 + tid; k < k0 + kc; k += blockDim.x)
+        xs[b * kc + (k - k0)] = (b < a.nb && k < k1) ? a.x_in[b * a.x_stride + k] : 0.f;
+    }
+    return;
+  }
+  const int n = a.norm_n;
+  float rd[NB];  // denominators of r (PRO_RESID)
+  if (a.pro == PRO_RESID) {
+    float ss[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      ss[b] = 0.f;
+      if (b < a.nb)
+        for (int k = tid; k < n; k += blockDim.x) {
+          float v = a.r_in[b * a.r_stride + k];
+          ss[b] += v * v;
+        }
+    }
+    block_sum<NB>(ss, red);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) rd[b] = rms_denom(ss[b], n, a.eps);
+  }
+  // New residual value at k (PRO_RESID), or the input itself (PRO_NORM).
+  auto xval = [&](int b, int k) -> float {
+    float x = a.x_in[b * a.x_stride + k];
+    if (a.pro == PRO_RESID) {
+      float r = a.r_in[b * a.r_stride + k];
+      x = (x + (r / rd[b]) * bf16f(a.g_r[k])) * a.lambda;
+    }
+    return x;
+  };
+  if (a.pro == PRO_RESID && blockIdx.x == 0) {
+    for (int b = 0; b < a.nb; ++b)
+      for (int k = tid; k < n; k += blockDim.x) a.x_out[b * a.x_stride + k] = xval(b, k);
+  }
+  float ad[NB];
+  if (a.g_a != nullptr) {
+    float ss[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      ss[b] = 0.f;
+      if (b < a.nb)
+        for (int k = tid; k < n; k += blockDim.x) {
+          float v = xval(b, k);
+          ss[b] += v * v;
+        }
+    }
+    block_sum<NB>(ss, red);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) ad[b] = rms_denom(ss[b], n, a.eps);
+  }
+  for (int b = 0; b < NB; ++b) {
+    for (int k = k0 + tid; k < k0 + kc; k += blockDim.x) {
+      float v = 0.f;
+      if (b < a.nb && k < k1) {
+        v = xval(b, k);
+        if (a.g_a != nullptr) v = (v / ad[b]) * bf16f(a.g_a[k]);
+      }
+      xs[b * kc + (k - k0)] = v;
+    }
+  }
+}
+
+template <int FMT, int R, int NB, int EPI>
+__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
+  using F = Fmt<FMT>;
+  extern __shared__ __align__(16) float smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = blockIdx.x / a.ksplit, ks = blockIdx.x % a.ksplit;
+  const int sg0 = ks * a.sg_per_cta;
+  const int sg1 = min(a.S, sg0 + a.sg_per_cta);
+  const int kc = a.sg_per_cta * F::SGK;          // smem chunk width
+  const int k0 = sg0 * F::SGK;
+  const int k1 = min(a.K, sg1 * F::SGK);
+  float* xs = smem;                               // [NB][kc]
+  float* red = smem + NB * kc;                    // [kGemvWarps][R*NB*32] (also block_sum)
+
+  // Issue this warp's first supergroup of weights before the prologue: weights never
+  // depend on activations.
+  const int rows_total = a.n_rb * 32;
+  int sg = sg0 + warp;
+  uint4 wbuf[R][8];
+  uint4 sbuf[R];
+  auto load_sg = [&](int s) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int rb = rg * R + r;
+      const uint4* base = a.qw + ((size_t)rb * a.tiles + (size_t)s * 8) * 32 + lane;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) wbuf[r][t] = __ldg(base + t * 32);
+      if constexpr (FMT == FMT_W4A16) sbuf[r] = __ldg(a.sc + ((size_t)rb * a.S + s) * 32 + lane);
+    }
+  };
+  if (sg < sg1) load_sg(sg);
+
+  gemv_prologue<NB>(a, xs, kc, k0, k1, red);
+  __syncthreads();
+
+  float2 acc[R][NB];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+
+  while (sg < sg1) {
+    const float* xsg = xs + (sg - sg0) * F::SGK;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        uint32_t s2 = 0;
+        if constexpr (FMT == FMT_W4A16) {
+          const uint32_t sw = (&sbuf[r].x)[t >> 1];
+          const uint32_t h = (t & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+          s2 = h | (h << 16);
+        }
+        tile_fma<FMT, NB>(wbuf[r][t], s2, xsg + t * F::TK, kc, acc[r]);
+      }
+    }
+    sg += kGemvWarps;
+    if (sg < sg1) load_sg(sg);
+  }
+
+  // Cross-warp reduction in fixed warp order.
+  constexpr int NV = R * NB * 32;
+  float* wred = red;  // [kGemvWarps][NV]
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) wred[warp * NV + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
+  __syncthreads();
+  float* fin = red + kGemvWarps * NV;  // [NV]
+  for (int i = threadIdx.x; i < NV; i += blockDim.x) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kGemvWarps; ++w) s += wred[w * NV + i];
+    fin[i] = s;
+  }
+  __syncthreads();
+
+  if (a.ksplit > 1) {
+    // partial -> scratch; the last CTA of the row group sums all partials in split order.
+    for (int i = threadIdx.x; i < NV; i += blockDim.x) {
+      const int b = (i / 32) % NB, r = i / (32 * NB), l = i % 32;
+      if (b < a.nb) a.part[((size_t)ks * a.nb + b) * rows_total + (rg * R + r) * 32 + l] = fin[i];
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int is_last;
+    if (threadIdx.x == 0) {
+      unsigned prev = atomicAdd(&a.counters[rg], 1u);
+      is_last = (prev == (unsigned)a.ksplit - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < NV; i += blockDim.x) {
+      const int b = (i / 32) % NB, r = i / (32 * NB), l = i % 32;
+      float s = 0.f;
+      if (b < a.nb)
+        for (int q = 0; q < a.ksplit; ++q)
+          s += ldcg(a.part + ((size_t)q * a.nb + b) * rows_total + (rg * R + r) * 32 + l);
+      fin[i] = s;
+    }
+    if (threadIdx.x == 0) a.counters[rg] = 0u;
+    __syncthreads();
+  }
+
+  // Epilogue (threads of warp 0 own lanes).
+  if constexpr (EPI == EPI_ARGMAX) {
+    __shared__ float bv[kMaxNB];
+    __shared__ int bi[kMaxNB];
+    if (warp == 0) {
+      for (int b = 0; b < a.nb; ++b) {
+        const int n = rg * 32 + lane;
+        float v = fin[b * 32 + lane];
+        int idx = n;
+        if (n >= a.n_valid) { v = __int_as_float(0x7fc00000); idx = 0x7fffffff; }
+        else if (a.logits) a.logits[(size_t)b * a.logits_stride + n] = v;
+        warp_argmax(v, idx);
+        if (lane == 0) { bv[b] = v; bi[b] = idx; }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < a.nb) {
+      a.am_val[threadIdx.x * gridDim.x + blockIdx.x] = bv[threadIdx.x];
+      a.am_idx[threadIdx.x * gridDim.x + blockIdx.x] = bi[threadIdx.x];
+    }
+    __threadfence();
+    __syncthreads();
+    __shared__ int is_last_am;
+    unsigned* cnt = a.counters + gridDim.x;  // one past the per-row-group counters
+    if (threadIdx.x == 0) is_last_am = (atomicAdd(cnt, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!is_last_am) return;
+    __threadfence();
+    __shared__ float rv[kGemvWarps];
+    __shared__ int ri[kGemvWarps];
+    for (int b = 0; b < a.nb; ++b) {
+      float v = __int_as_float(0x7fc00000);
+      int idx = 0x7fffffff;
+      for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
+        float cv = ldcg(a.am_val + b * gridDim.x + c);
+        int ci = __ldcg(a.am_idx + b * gridDim.x + c);
+        if (argmax_better(cv, ci, v, idx)) { v = cv; idx = ci; }
+      }
+      warp_argmax(v, idx);
+      if (lane == 0) { rv[warp] = v; ri[warp] = idx; }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < kGemvWarps; ++w)
+          if (argmax_better(rv[w], ri[w], rv[0], ri[0])) { rv[0] = rv[w]; ri[0] = ri[w]; }
+        a.next_ids[b] = ri[0] == 0x7fffffff ? 0 : ri[0];
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) *cnt = 0u;
+  } else {
+    if (warp != 0) return;
+    for (int b = 0; b < a.nb; ++b) {
+      if constexpr (EPI == EPI_GEGLU) {
+        const int n = rg * 32 + lane;  // R == 2: block 0 = gate rows, block 1 = up rows
+        if (n < a.n_valid) {
+          const float g = fin[(0 * NB + b) * 32 + lane], u = fin[(1 * NB + b) * 32 + lane];
+          a.y[(size_t)b * a.y_stride + n] = gelu_tanh(g) * u;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const int n = (rg * R + r) * 32 + lane;
+          if (n >= a.n_valid) continue;
+          float v = fin[(r * NB + b) * 32 + lane];
+          if constexpr (EPI == EPI_PLE) v = gelu_tanh(v) * a.ple[(size_t)b * a.ple_stride + n];
+          a.y[(size_t)b * a.y_stride + n] = v;
+        }
+      }
+    }
+  }
+}
+
+// Shared memory bytes of one launch.
+template <int FMT, int R, int NB>
+inline size_t gemv_smem_bytes(int sg_per_cta) {
+  const int kc = sg_per_cta * Fmt<FMT>::SGK;
+  const int nv = R * NB * 32;
+  size_t red = (size_t)(kGemvWarps + 1) * nv;
+  if (red < 32 * NB) red = 32 * NB;
+  return ((size_t)NB * kc + red) * sizeof(float);
+}
+
+}  // namespace g4

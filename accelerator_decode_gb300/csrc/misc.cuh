@@ -1,0 +1,181 @@
+// Embedding gather, per-layer-embedding combine, weight repacking, standalone argmax.
+#pragma once
+#include "common.cuh"
+
+namespace g4 {
+
+// x0[b] = E[t_b] * sqrt(H);  tok[b] = T_ple[t_b] * sqrt(P)   (fp32)
+// Token ids come from tokens[b] or, with idx != nullptr, tokens[idx[b]].
+// "Porting Gemma 4 E2B to SGLang-JAX", Step 3: tok = embed_tokens_per_layer(ids) * ple_dim**0.5.
+struct EmbedArgs {
+  const int* tokens;
+  const int* idx;
+  const __nv_bfloat16* embed;      // [V][H]
+  const __nv_bfloat16* ple_table;  // [V][LP]
+  int V, H, LP;
+  float sqrt_h, sqrt_p;
+  float* x0;   // [nb][H]
+  float* tok;  // [nb][LP]
+  int* err;
+};
+
+__global__ void embed_kernel(const EmbedArgs a) {
+  const int b = blockIdx.x;
+  int t = a.idx ? a.tokens[a.idx[b]] : a.tokens[b];
+  if (t < 0 || t >= a.V) {
+    if (threadIdx.x == 0) set_err(a.err, G4_DEV_BAD_TOKEN);
+    t = 0;
+  }
+  const __nv_bfloat16* e = a.embed + (size_t)t * a.H;
+  for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.x0[(size_t)b * a.H + k] = bf16f(e[k]) * a.sqrt_h;
+  const __nv_bfloat16* p = a.ple_table + (size_t)t * a.LP;
+  for (int k = threadIdx.x; k < a.LP; k += blockDim.x) a.tok[(size_t)b * a.LP + k] = bf16f(p[k]) * a.sqrt_p;
+}
+
+// ple[b][l] = (RMSNorm(pr[b][l] * H^-1/2) * g + tok[b][l]) * 2^-1/2, one block per (b, l).
+// "Porting Gemma 4 E2B to SGLang-JAX", Step 3 (per-layer projection norm and the combine).
+__global__ void ple_combine_kernel(const float* pr, const float* tok, const __nv_bfloat16* g, int L, int P,
+                                   float inv_sqrt_h, float inv_sqrt2, float eps, float* ple) {
+  __shared__ float red[32];
+  const int b = blockIdx.y, l = blockIdx.x;
+  const size_t base = ((size_t)b * L + l) * P;
+  float ss[1] = {0.f};
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    const float v = pr[base + i] * inv_sqrt_h;
+    ss[0] += v * v;
+  }
+  block_sum<1>(ss, red);
+  const float den = rms_denom(ss[0], P, eps);
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    const float v = pr[base + i] * inv_sqrt_h;
+    ple[base + i] = ((v / den) * bf16f(g[i]) + tok[base + i]) * inv_sqrt2;
+  }
+}
+
+// ------------------------------------------------------------------------------ repacking
+// One destination 32-row block: `w` points at its first source row (nullptr = zero block),
+// `s` at its first scale row (W4A16), `rows` valid rows (<= 32).
+struct RbSrc {
+  const void* w;
+  const void* s;
+  int rows;
+  int pad;
+};
+
+// Canonical int4 (k at word k/8, bits 4*(k%8), two's complement) -> tiled offset-binary.
+__global__ void repack_int4_kernel(const RbSrc* srcs, int n_rb, int K, int tiles, uint4* qw) {
+  const size_t total = (size_t)n_rb * tiles * 32;
+  const int G = K / 32;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int lane = i % 32;
+    const int g = (i / 32) % tiles;
+    const int rb = i / (32 * (size_t)tiles);
+    const RbSrc s = srcs[rb];
+    uint32_t out[4] = {0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u};  // q = 0
+    if (s.w != nullptr && lane < s.rows && g < G) {
+      const uint32_t* row = reinterpret_cast<const uint32_t*>(s.w) + (size_t)lane * (K / 8);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t c = row[4 * g + m];
+        uint32_t o = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t nib = ((c >> (4 * e)) & 0xFu) ^ 0x8u;
+          const int pos = (e & 1) ? 16 + 4 * (e >> 1) : 4 * (e >> 1);
+          o |= nib << pos;
+        }
+        out[m] = o;
+      }
+    }
+    qw[i] = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// bf16 scales [N][K/32] -> sc[(rb * S + sg) * 32 + lane] = 8 scales of groups 8sg..8sg+7.
+__global__ void repack_scales_kernel(const RbSrc* srcs, int n_rb, int K, int S, uint4* sc) {
+  const size_t total = (size_t)n_rb * S * 32;
+  const int G = K / 32;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int lane = i % 32;
+    const int sg = (i / 32) % S;
+    const int rb = i / (32 * (size_t)S);
+    const RbSrc s = srcs[rb];
+    uint16_t v[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int g = sg * 8 + t;
+      v[t] = 0;
+      if (s.s != nullptr && lane < s.rows && g < G)
+        v[t] = reinterpret_cast<const uint16_t*>(s.s)[(size_t)lane * G + g];
+    }
+    sc[i] = make_uint4(v[0] | (uint32_t(v[1]) << 16), v[2] | (uint32_t(v[3]) << 16),
+                       v[4] | (uint32_t(v[5]) << 16), v[6] | (uint32_t(v[7]) << 16));
+  }
+}
+
+// bf16 row-major [N][K] -> tiled: qw[(rb * tiles + c) * 32 + lane] = row k in [8c, 8c+8).
+__global__ void repack_bf16_kernel(const RbSrc* srcs, int n_rb, int K, int tiles, uint4* qw) {
+  const size_t total = (size_t)n_rb * tiles * 32;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int lane = i % 32;
+    const int c = (i / 32) % tiles;
+    const int rb = i / (32 * (size_t)tiles);
+    const RbSrc s = srcs[rb];
+    uint4 out = make_uint4(0, 0, 0, 0);
+    if (s.w != nullptr && lane < s.rows && 8 * c < K)
+      out = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(s.w) + (size_t)lane * K + 8 * c);
+    qw[i] = out;
+  }
+}
+
+// ------------------------------------------------------------------------ standalone argmax
+// Block partials over column chunks, then the last block reduces (same scheme as the lm_head).
+__global__ void argmax_rows_kernel(const float* logits, int n_cols, int chunk, float* pv, int* pi,
+                                   unsigned* counter, int* ids) {
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  float v = __int_as_float(0x7fc00000);
+  int idx = 0x7fffffff;
+  const int c0 = c * chunk, c1 = min(n_cols, c0 + chunk);
+  for (int j = c0 + threadIdx.x; j < c1; j += blockDim.x) {
+    const float x = logits[(size_t)row * n_cols + j];
+    if (argmax_better(x, j, v, idx)) { v = x; idx = j; }
+  }
+  warp_argmax(v, idx);
+  if (lane == 0) { sv[warp] = v; si[warp] = idx; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < nw; ++w)
+      if (argmax_better(sv[w], si[w], sv[0], si[0])) { sv[0] = sv[w]; si[0] = si[w]; }
+    pv[row * gridDim.x + c] = sv[0];
+    pi[row * gridDim.x + c] = si[0];
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int is_last;
+  if (threadIdx.x == 0) is_last = atomicAdd(&counter[row], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  v = __int_as_float(0x7fc00000);
+  idx = 0x7fffffff;
+  for (int j = threadIdx.x; j < (int)gridDim.x; j += blockDim.x) {
+    const float x = ldcg(pv + row * gridDim.x + j);
+    const int xi = __ldcg(pi + row * gridDim.x + j);
+    if (argmax_better(x, xi, v, idx)) { v = x; idx = xi; }
+  }
+  warp_argmax(v, idx);
+  __syncthreads();
+  if (lane == 0) { sv[warp] = v; si[warp] = idx; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < nw; ++w)
+      if (argmax_better(sv[w], si[w], sv[0], si[0])) { sv[0] = sv[w]; si[0] = si[w]; }
+    ids[row] = si[0] == 0x7fffffff ? 0 : si[0];
+    counter[row] = 0u;
+  }
+}
+
+}  // namespace g4

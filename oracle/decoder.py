@@ -365,9 +365,11 @@ class Oracle:
         return o
 
     # -- one decode step ----------------------------------------------------------------------
-    def step(self, slots, tokens, positions):
+    def step(self, slots, tokens, positions, trace=None):
         """One token per sequence: tokens[i] at positions[i] of cache slot slots[i].
-        Writes the owning layers' K/V at that position and returns logits [n, V]."""
+        Writes the owning layers' K/V at that position and returns logits [n, V].
+        trace (optional dict) receives per layer the attention output and the residual
+        stream after the layer: trace[("attn", l)], trace[("x", l)]."""
         slots = np.asarray(slots)
         tokens = np.asarray(tokens)
         positions = np.asarray(positions)
@@ -382,9 +384,13 @@ class Oracle:
                 self.K[l][slots, positions] = k
                 self.Vc[l][slots, positions] = v
             o = self.attention_layer(l, q, slots, positions)
+            if trace is not None:
+                trace[("attn", l)] = o.reshape(len(tokens), -1).copy()
             x = x + rmsnorm(o.reshape(len(tokens), -1) @ self.W[(l, "o")].T, g["post_attn_norm"],
                             self.eps)
             x = self._mlp_ple(l, x, ple[:, l])
+            if trace is not None:
+                trace[("x", l)] = x.copy()
         return self.final_logits(x)
 
     # -- whole sequences ----------------------------------------------------------------------

@@ -1,0 +1,237 @@
+"""End-to-end parity of the CUDA decode step with the CPU oracle (tiny shapes), through the C ABI.
+
+Bar: greedy ids identical; final logits max|d| <= 3e-2 and cosine >= 0.999; per-layer outputs
+(attention output, residual stream) within rtol 1e-2 of the oracle's.  Where the oracle's
+top-2 gap at a step is below GAP_TIE the two argmaxes may legitimately differ (a near tie:
+fp32 noise flips bf16 K/V roundings, moving logits by ~1e-4); the tests report such steps and
+continue teacher-forced on the oracle's token."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+LOGIT_TOL = 3e-2
+COS_MIN = 0.999
+GAP_TIE = 2e-3
+
+
+@pytest.fixture(scope="module")
+def rt():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from accelerator_decode_gb300 import runtime
+    return runtime
+
+
+def _cos(a, b):
+    a, b = a.astype(np.float64).ravel(), b.astype(np.float64).ravel()
+    return float(a @ b / np.linalg.norm(a) / np.linalg.norm(b))
+
+
+def gpu_generate(dec, prompts, n_out, slots=None, teacher=None, want_logits=True):
+    """Greedy decode on the GPU.  teacher[i] (optional): token sequence to feed instead of
+    the GPU's own argmax (teacher forcing).  Returns tokens [n, n_out], logits [n_out, n, V]."""
+    n = len(prompts)
+    slots = list(range(n)) if slots is None else list(slots)
+    nxt, lg = dec.prefill(slots, prompts, want_logits=want_logits)
+    torch.cuda.synchronize()
+    toks = [nxt.cpu().numpy().copy()]
+    logits = [lg.cpu().numpy().copy()] if want_logits else []
+    d_slots = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    pos = torch.tensor([len(p) for p in prompts], dtype=torch.int32, device="cuda")
+    tok = nxt.clone()
+    out = torch.empty(n, dtype=torch.int32, device="cuda")
+    lgt = torch.empty(n, dec.cfg["vocab"], dtype=torch.float32, device="cuda") if want_logits else None
+    for s in range(1, n_out):
+        if teacher is not None:
+            tok.copy_(torch.from_numpy(np.asarray(teacher[:, s - 1], np.int32)).cuda())
+        dec.decode_step(d_slots, tok, pos, out, lgt)
+        torch.cuda.synchronize()
+        toks.append(out.cpu().numpy().copy())
+        if want_logits:
+            logits.append(lgt.cpu().numpy().copy())
+        tok.copy_(out)
+        pos += 1
+    return np.stack(toks, 1), (np.stack(logits) if want_logits else None)
+
+
+def check_parity(ref, toks, logits, label):
+    """Free-running comparison; a divergence is allowed only at a near tie of the oracle."""
+    n, n_out = toks.shape
+    for i in range(n):
+        same = np.cumprod(toks[i] == ref["tokens"][i]).sum()
+        if same < n_out:
+            gap = ref["gaps"][same, i]
+            assert gap < GAP_TIE, f"{label}: seq {i} diverges at step {same} with top-2 gap {gap}"
+            pytest.skip(f"{label}: near tie (gap {gap:.1e}) at step {same}; see teacher-forced test")
+    err = np.max(np.abs(logits[-1] - ref["logits"][-1]))
+    assert err <= LOGIT_TOL, (label, err)
+    for i in range(n):
+        assert _cos(logits[-1][i], ref["logits"][-1][i]) >= COS_MIN
+    return err
+
+
+CASES = [("tiny", "bf16"), ("tiny", "w4a16"), ("tiny10", "bf16"), ("tiny10", "w4a16")]
+
+
+@pytest.mark.parametrize("name,fmt", CASES)
+def test_tiny_greedy_matches_oracle(rt, name, fmt):
+    cfg = synth.get_config(name)
+    w = synth.make_weights(cfg, fmt, seed=0, gain_std=0.1, layer_scale_std=0.05)
+    prompts = synth.make_prompts(cfg["vocab"], 1, 16, seed=0)
+    ref = oracle.Oracle(cfg, w, max_batch=1, max_context=64).generate(prompts, 16, keep_logits=True)
+    dec = rt.Decoder(cfg, w, max_batch=1, max_context=64)
+    toks, logits = gpu_generate(dec, list(prompts), 16)
+    assert dec.device_error()[1] == 0
+    dec.close()
+    check_parity(ref, toks, logits, f"{name}/{fmt}")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "w4a16"])
+def test_teacher_forced_every_step(rt, fmt):
+    """Feed the oracle's tokens: every step's logits and argmax must agree (argmax only
+    where the oracle's top-2 gap exceeds the near-tie bound)."""
+    cfg = synth.get_config("tiny10")
+    w = synth.make_weights(cfg, fmt, seed=11)
+    prompts = synth.make_prompts(cfg["vocab"], 2, 12, seed=4)
+    ref = oracle.Oracle(cfg, w, max_batch=2, max_context=64).generate(prompts, 24, keep_logits=True)
+    dec = rt.Decoder(cfg, w, max_batch=2, max_context=64)
+    toks, logits = gpu_generate(dec, list(prompts), 24, teacher=ref["tokens"])
+    dec.close()
+    assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL
+    ok = ref["gaps"].T > GAP_TIE
+    assert np.all((toks == ref["tokens"]) | ~ok)
+
+
+def test_window_binds(rt):
+    """A sliding window shorter than the context (8 keys with 16+ positions)."""
+    cfg = dict(synth.get_config("tiny10"), sliding_window=8)
+    w = synth.make_weights(cfg, "w4a16", seed=2)
+    prompts = synth.make_prompts(cfg["vocab"], 1, 16, seed=1)
+    ref = oracle.Oracle(cfg, w, max_batch=1, max_context=64).generate(prompts, 12, keep_logits=True)
+    dec = rt.Decoder(cfg, w, max_batch=1, max_context=64)
+    toks, logits = gpu_generate(dec, list(prompts), 12, teacher=ref["tokens"])
+    dec.close()
+    assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL
+
+
+def test_per_layer_trace_within_rtol(rt):
+    """Each kernel's output (attention output and residual stream per layer) against the
+    oracle's intermediates at the last prefill position."""
+    cfg = synth.get_config("tiny10")
+    w = synth.make_weights(cfg, "w4a16", seed=5, gain_std=0.1)
+    prompt = synth.make_prompts(cfg["vocab"], 1, 10, seed=3)
+    o = oracle.Oracle(cfg, w, max_batch=1, max_context=32)
+    o.prefill([0], prompt[:, :9])
+    tr = {}
+    o.step([0], prompt[:, 9], [9], trace=tr)
+    dec = rt.Decoder(cfg, w, max_batch=1, max_context=32)
+    t = dec.set_trace(True)
+    dec.prefill([0], [prompt[0]])
+    torch.cuda.synchronize()
+    t = t.cpu().numpy()
+    dec.close()
+    for l in range(cfg["num_layers"]):
+        a = tr[("attn", l)][0]
+        np.testing.assert_allclose(t[l, 0, 0, :a.size], a, rtol=1e-2, atol=1e-3 * np.max(np.abs(a)))
+        x = tr[("x", l)][0]
+        np.testing.assert_allclose(t[l, 1, 0, :x.size], x, rtol=1e-2, atol=1e-3 * np.max(np.abs(x)))
+
+
+def test_ragged_batch_slots_and_append(rt):
+    """Three sequences of different lengths in permuted slots, then an append-prefill
+    (start_pos > 0) and batched decode steps at different positions."""
+    cfg = synth.get_config("tiny10")
+    w = synth.make_weights(cfg, "bf16", seed=8)
+    lens = [5, 12, 9]
+    prompts = [synth.make_prompts(cfg["vocab"], 1, L, seed=20 + i)[0] for i, L in enumerate(lens)]
+    extra = [synth.make_prompts(cfg["vocab"], 1, 4, seed=40 + i)[0] for i in range(3)]
+    slots = [2, 0, 3]
+    dec = rt.Decoder(cfg, w, max_batch=4, max_context=48)
+    nxt, lg = dec.prefill(slots, prompts, want_logits=True)
+    nxt2, lg2 = dec.prefill(slots, extra, start_pos=lens, want_logits=True)
+    d_slots = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    pos = torch.tensor([L + 4 for L in lens], dtype=torch.int32, device="cuda")
+    tok = nxt2.clone()
+    out = torch.empty(3, dtype=torch.int32, device="cuda")
+    lgs = torch.empty(3, cfg["vocab"], dtype=torch.float32, device="cuda")
+    steps = []
+    for s in range(3):
+        dec.decode_step(d_slots, tok, pos, out, lgs)
+        torch.cuda.synchronize()
+        steps.append((out.cpu().numpy().copy(), lgs.cpu().numpy().copy()))
+        tok.copy_(out)
+        pos += 1
+    assert dec.device_error()[1] == 0
+    dec.close()
+    for i in range(3):
+        o = oracle.Oracle(cfg, w, max_batch=1, max_context=48)
+        l1 = o.prefill([0], prompts[i][None])
+        l2 = o.prefill([0], extra[i][None], start_pos=[lens[i]])
+        np.testing.assert_allclose(lg.cpu().numpy()[i], l1[0], atol=LOGIT_TOL)
+        np.testing.assert_allclose(lg2.cpu().numpy()[i], l2[0], atol=LOGIT_TOL)
+        t = int(nxt2.cpu().numpy()[i])
+        assert t == int(np.argmax(l2[0]))
+        for s in range(3):
+            ls = o.step([0], [t], [lens[i] + 4 + s])
+            np.testing.assert_allclose(steps[s][1][i], ls[0], atol=LOGIT_TOL)
+            t = int(steps[s][0][i])
+
+
+def test_batch_larger_than_gemv_chunk(rt):
+    """Batch 6 crosses the 4-row GEMV chunk; every sequence must match its oracle run."""
+    cfg = synth.get_config("tiny")
+    w = synth.make_weights(cfg, "w4a16", seed=9)
+    prompts = synth.make_prompts(cfg["vocab"], 6, 8, seed=6)
+    ref = oracle.Oracle(cfg, w, max_batch=6, max_context=32).generate(prompts, 6, keep_logits=True)
+    dec = rt.Decoder(cfg, w, max_batch=6, max_context=32)
+    toks, logits = gpu_generate(dec, list(prompts), 6, teacher=ref["tokens"])
+    dec.close()
+    assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL
+
+
+def test_rerun_is_bitwise_deterministic(rt):
+    cfg = synth.get_config("tiny")
+    w = synth.make_weights(cfg, "w4a16", seed=1)
+    prompts = list(synth.make_prompts(cfg["vocab"], 2, 8, seed=2))
+    runs = []
+    for _ in range(2):
+        dec = rt.Decoder(cfg, w, max_batch=2, max_context=32)
+        runs.append(gpu_generate(dec, prompts, 5))
+        dec.close()
+    assert np.array_equal(runs[0][0], runs[1][0]) and np.array_equal(runs[0][1], runs[1][1])
+
+
+def test_errors_host_and_device(rt):
+    from accelerator_decode_gb300 import g4
+    cfg = synth.get_config("tiny")
+    w = synth.make_weights(cfg, "bf16", seed=1)
+    dec = rt.Decoder(cfg, w, max_batch=2, max_context=16)
+    p = synth.make_prompts(cfg["vocab"], 1, 4, seed=0)[0]
+    with pytest.raises(g4.G4Error) as e:
+        dec.prefill([0], [np.zeros(17, np.int32)])
+    assert e.value.status == g4.G4_ERR_CONTEXT_OVERFLOW
+    with pytest.raises(g4.G4Error) as e:
+        dec.prefill([1, 1], [p, p])
+    assert e.value.status == g4.G4_ERR_INVALID_ARG
+    with pytest.raises(g4.G4Error) as e:
+        dec.prefill([5], [p])
+    assert e.value.status == g4.G4_ERR_INVALID_ARG
+    d = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    out = torch.empty(1, dtype=torch.int32, device="cuda")
+    dec.decode_step(d([0]), d([cfg["vocab"] + 3]), d([0]), out)
+    st, word = dec.device_error()
+    assert st == g4.G4_ERR_DEVICE_CHECK and word & g4.G4_DEV_BAD_TOKEN
+    dec.decode_step(d([0]), d([1]), d([16]), out)
+    st, word = dec.device_error()
+    assert word & g4.G4_DEV_BAD_POSITION
+    assert dec.device_error() == (g4.G4_OK, 0)     # read clears the word
+    # the handle stays usable after device-side check failures
+    dec.prefill([0], [p])
+    torch.cuda.synchronize()
+    assert dec.device_error() == (g4.G4_OK, 0)
+    dec.close()
