@@ -354,9 +354,37 @@ int attn_nsplit(int sms, int nq, int hpc, int nb, int max_keys) {
   return std::max(1, std::min(ns, 64));
 }
 
+// ------------------------------------------------------------------------------- profiler
+// Optional CUDA-event bracketing of every launch of a (non-captured) step, by phase name.
+struct Prof {
+  struct Rec {
+    std::string name;
+    double bytes;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  cudaStream_t st = nullptr;
+  void begin(const char* name, double bytes) {
+    Rec r{name, bytes, nullptr, nullptr};
+    cudaEventCreate(&r.a);
+    cudaEventCreate(&r.b);
+    cudaEventRecord(r.a, st);
+    recs.push_back(r);
+  }
+  void end() { cudaEventRecord(recs.back().b, st); }
+  ~Prof() {
+    for (Rec& r : recs) { cudaEventDestroy(r.a); cudaEventDestroy(r.b); }
+  }
+};
+struct ProfScope {
+  Prof* p;
+  ProfScope(Prof* p_, const char* name, double bytes) : p(p_) { if (p) p->begin(name, bytes); }
+  ~ProfScope() { if (p) p->end(); }
+};
+
 // ------------------------------------------------------------------------------- the step
 g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens, const int* d_idx,
-                   const int* d_pos, int* d_next, float* d_logits) {
+                   const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr) {
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
   const float eps = c.rms_eps;
@@ -364,8 +392,12 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
 
   EmbedArgs ea{d_tokens, d_idx, h->embed, h->ple_table, c.vocab, H, LP,
                (float)std::sqrt((double)H), (float)std::sqrt((double)P), h->x0, h->tok, h->err};
-  embed_kernel<<<n, 256, 0, st>>>(ea);
   {
+    ProfScope ps(prof, "embed", (double)n * (H + LP) * 2);
+    embed_kernel<<<n, 256, 0, st>>>(ea);
+  }
+  {
+    ProfScope ps(prof, "gemv.ple_model_proj", (double)h->pmp.bytes);
     GemvIO io;
     io.pro = PRO_PLAIN;
     io.x_in = h->x0;
@@ -374,8 +406,11 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
     io.y_stride = LP;
     run_gemv(h->pmp, EPI_STORE, io, n, eps, s, st);
   }
-  ple_combine_kernel<<<dim3(L, n), std::min(256, std::max(32, P)), 0, st>>>(
-      h->pr, h->tok, h->g_ppn, L, P, (float)(1.0 / std::sqrt((double)H)), (float)(1.0 / std::sqrt(2.0)), eps, h->ple);
+  {
+    ProfScope ps(prof, "ple_combine", 0.0);
+    ple_combine_kernel<<<dim3(L, n), std::min(256, std::max(32, P)), 0, st>>>(
+        h->pr, h->tok, h->g_ppn, L, P, (float)(1.0 / std::sqrt((double)H)), (float)(1.0 / std::sqrt(2.0)), eps, h->ple);
+  }
 
   float* cur = h->x0;
   auto next_x = [&]() { return cur == h->xb[0] ? h->xb[1] : h->xb[0]; };
@@ -402,7 +437,10 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       }
       io.y = h->qkv;
       io.y_stride = Y.qkv.n_valid;
-      run_gemv(Y.qkv, EPI_STORE, io, n, eps, s, st);
+      {
+        ProfScope ps(prof, "gemv.qkv", (double)Y.qkv.bytes);
+        run_gemv(Y.qkv, EPI_STORE, io, n, eps, s, st);
+      }
       if (l > 0) {
         cur = io.x_out;
         if (h->trace)
@@ -439,6 +477,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.ws_o = h->attn_o;
       a.counters = h->attn_cnt;
       a.err = h->err;
+      ProfScope ps(prof, Y.full ? "attn.full" : "attn.sliding", 0.0);
       switch (Y.d) {
         case 64: launch_attn_d<64>(a, hpc, n, st); break;
         case 128: launch_attn_d<128>(a, hpc, n, st); break;
@@ -457,6 +496,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.x_stride = nqd;
       io.y = h->r_attn;
       io.y_stride = H;
+      ProfScope ps(prof, "gemv.o", (double)Y.o.bytes);
       run_gemv(Y.o, EPI_STORE, io, n, eps, s, st);
     }
     {  // gate/up
@@ -473,7 +513,10 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.x_out = next_x();
       io.y = h->act;
       io.y_stride = Y.F;
-      run_gemv(Y.gu, EPI_GEGLU, io, n, eps, s, st);
+      {
+        ProfScope ps(prof, "gemv.gate_up", (double)Y.gu.bytes);
+        run_gemv(Y.gu, EPI_GEGLU, io, n, eps, s, st);
+      }
       cur = io.x_out;
     }
     {  // down
@@ -483,6 +526,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.x_stride = Y.F;
       io.y = h->r_mlp;
       io.y_stride = H;
+      ProfScope ps(prof, "gemv.down", (double)Y.down.bytes);
       run_gemv(Y.down, EPI_STORE, io, n, eps, s, st);
     }
     {  // PLE gate
@@ -501,7 +545,10 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y_stride = P;
       io.ple = h->ple + (size_t)l * P;
       io.ple_stride = LP;
-      run_gemv(Y.pg, EPI_PLE, io, n, eps, s, st);
+      {
+        ProfScope ps(prof, "gemv.ple_gate", (double)Y.pg.bytes);
+        run_gemv(Y.pg, EPI_PLE, io, n, eps, s, st);
+      }
       cur = io.x_out;
     }
     {  // PLE proj
@@ -511,6 +558,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.x_stride = P;
       io.y = h->r_ple;
       io.y_stride = H;
+      ProfScope ps(prof, "gemv.ple_proj", (double)Y.pp.bytes);
       run_gemv(Y.pp, EPI_STORE, io, n, eps, s, st);
     }
   }
@@ -530,7 +578,10 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
     io.logits = d_logits;
     io.logits_stride = c.vocab;
     io.next_ids = d_next;
-    run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, st);
+    {
+      ProfScope ps(prof, "gemv.lm_head_argmax", (double)h->lm.bytes);
+      run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, st);
+    }
     if (h->trace)
       for (int i = 0; i < n; ++i)
         cudaMemcpyAsync(h->trace + ((size_t)((L - 1) * 2 + 1) * c.max_batch + i) * ts, io.x_out + (size_t)i * H,
@@ -876,6 +927,49 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
                            (size_t)c.vocab * sizeof(float), cudaMemcpyDeviceToDevice, st));
     }
   }
+  return G4_OK;
+}
+
+g4_status g4_profile_step(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_t* d_slots,
+                          const int32_t* d_tokens, const int32_t* d_positions, int32_t* d_next_ids, float* d_logits,
+                          int32_t repeats, g4_phase_stat* stats, int32_t max_stats, int32_t* n_stats) {
+  if (!h || !d_slots || !d_tokens || !d_positions || !d_next_ids || !stats || !n_stats || repeats < 1)
+    return G4_ERR_INVALID_ARG;
+  if (n_seq < 1 || n_seq > h->cfg.max_batch) return G4_ERR_INVALID_ARG;
+  CK(cudaSetDevice(h->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Prof prof;
+  prof.st = st;
+  float* saved_trace = h->trace;
+  h->trace = nullptr;
+  g4_status s = G4_OK;
+  for (int r = 0; r < repeats && s == G4_OK; ++r)
+    s = run_step(h, st, n_seq, d_slots, d_tokens, nullptr, d_positions, d_next_ids, d_logits, &prof);
+  h->trace = saved_trace;
+  if (s != G4_OK) return s;
+  CK(cudaStreamSynchronize(st));
+  std::vector<std::string> order;
+  std::map<std::string, g4_phase_stat> agg;
+  for (const Prof::Rec& r : prof.recs) {
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, r.a, r.b));
+    auto it = agg.find(r.name);
+    if (it == agg.end()) {
+      g4_phase_stat z{};
+      snprintf(z.name, sizeof z.name, "%s", r.name.c_str());
+      it = agg.emplace(r.name, z).first;
+      order.push_back(r.name);
+    }
+    it->second.launches += 1;
+    it->second.ms_total += ms;
+    it->second.bytes_total += r.bytes;
+  }
+  int k = 0;
+  for (const std::string& nm : order) {
+    if (k >= max_stats) break;
+    stats[k++] = agg[nm];
+  }
+  *n_stats = k;
   return G4_OK;
 }
 

@@ -56,6 +56,11 @@ class g4_weights(ctypes.Structure):
                 ("layers", POINTER(g4_layer_weights))]
 
 
+class g4_phase_stat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", c_int32), ("ms_total", ctypes.c_double),
+                ("bytes_total", ctypes.c_double)]
+
+
 class G4Error(RuntimeError):
     def __init__(self, status, where):
         self.status = status
@@ -80,6 +85,8 @@ def _load():
         "g4_get_device_error": (c_int, [P, P, POINTER(c_int32)]),
         "g4_set_trace": (c_int, [P, P, c_int64]),
         "g4_device_bytes": (c_int64, [P]),
+        "g4_profile_step": (c_int, [P, P, c_int32, P, P, P, P, P, c_int32, POINTER(g4_phase_stat), c_int32,
+                                    POINTER(c_int32)]),
         "g4_free": (None, [P]),
         "g4_status_string": (ctypes.c_char_p, [c_int]),
         "g4_last_cuda_error": (ctypes.c_char_p, []),
@@ -155,6 +162,16 @@ def g4_get_device_error(h, stream):
 
 def g4_set_trace(h, d_trace, capacity):
     check(lib.g4_set_trace(h, d_trace, capacity), "g4_set_trace")
+
+
+def g4_profile_step(h, stream, n_seq, d_slots, d_tokens, d_positions, d_next_ids, d_logits, repeats):
+    """Per-phase timing: list of dicts(name, launches, ms_total, bytes_total)."""
+    arr = (g4_phase_stat * 64)()
+    n = c_int32(0)
+    check(lib.g4_profile_step(h, stream, n_seq, d_slots, d_tokens, d_positions, d_next_ids, d_logits, repeats,
+                              arr, 64, ctypes.byref(n)), "g4_profile_step")
+    return [dict(name=arr[i].name.decode(), launches=arr[i].launches, ms_total=arr[i].ms_total,
+                 bytes_total=arr[i].bytes_total) for i in range(n.value)]
 
 
 def g4_free(h):

@@ -52,7 +52,7 @@ class Decoder:
             else:
                 t = _dev(x["packed"], self.device)
                 s = _dev(x["scales"], self.device)
-                tmp += [t, s]
+                tmp.extend([t, s])
                 lin.w, lin.scales = t.data_ptr(), s.data_ptr()
             return lin
 
@@ -98,6 +98,10 @@ class Decoder:
         n = d_tokens.numel()
         _g4.g4_decode_step(self.h, stream_handle(stream), n, _ptr(d_slots), _ptr(d_tokens), _ptr(d_positions),
                            _ptr(d_next), _ptr(d_logits))
+
+    def profile_step(self, d_slots, d_tokens, d_positions, d_next, d_logits=None, repeats=1, stream=None):
+        return _g4.g4_profile_step(self.h, stream_handle(stream), d_tokens.numel(), _ptr(d_slots), _ptr(d_tokens),
+                                   _ptr(d_positions), _ptr(d_next), _ptr(d_logits), repeats)
 
     def device_error(self, stream=None):
         return _g4.g4_get_device_error(self.h, stream_handle(stream))

@@ -158,6 +158,24 @@ g4_status g4_get_device_error(g4_handle* h, g4_stream stream, int32_t* word_out)
  * num_layers * 2 * max_batch * stride floats; pass NULL to stop.  Errors: INVALID_ARG. */
 g4_status g4_set_trace(g4_handle* h, float* d_trace, int64_t capacity_floats);
 
+/* Per-phase timing of the decode step (profiling).  Runs `repeats` decode steps with the
+ * same arguments as g4_decode_step, launched directly (not from a graph) with a CUDA event
+ * pair on `stream` around every phase launch, synchronises, and fills one entry per phase
+ * name in first-launch order: launches, total milliseconds between its events, and the
+ * bytes of weights its launches stream (the KV bytes of attention phases are not counted:
+ * the host does not know the positions).  Each repeat rewrites the same K/V rows, so the
+ * cache state is that of one step.  Errors: INVALID_ARG. */
+typedef struct g4_phase_stat {
+  char name[32];
+  int32_t launches;
+  double ms_total;
+  double bytes_total;
+} g4_phase_stat;
+g4_status g4_profile_step(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_t* d_slots,
+                          const int32_t* d_tokens, const int32_t* d_positions, int32_t* d_next_ids,
+                          float* d_logits, int32_t repeats, g4_phase_stat* stats, int32_t max_stats,
+                          int32_t* n_stats);
+
 /* Bytes of device memory the handle owns (weights copies, KV cache, workspaces). */
 int64_t g4_device_bytes(const g4_handle* h);
 
