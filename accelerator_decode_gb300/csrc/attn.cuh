@@ -8,9 +8,9 @@
 //   eight agents", The engine: kv_share_map, static cache written in place).
 //   keys j in [lo, p], lo = 0 (full) or max(0, p - W + 1) (sliding window W);
 //   s_j = scale * q_h . K_j; o_h = sum_j softmax(s)_j V_j  (fp32, max-subtracted).
-// The visible keys are cut into nsplit chunks (one CTA each) processed in tiles of 32 with
-// an online softmax; the last CTA of a (sequence, head group) merges the chunks with their
-// log-sum-exp weights.
+// The visible keys are cut into nsplit chunks (one CTA each), staged through shared memory
+// in tiles of 32 keys (2-stage cp.async pipeline) and reduced with an online softmax; the
+// last CTA of a (sequence, head group) merges the chunks with their log-sum-exp weights.
 #pragma once
 #include "common.cuh"
 
@@ -40,6 +40,7 @@ struct AttnArgs {
   float* out;              // [nb][out_stride]
   int out_stride;
   int nsplit;
+  int nstage;              // 1 or 2 tile buffers
   float* ws_ml;            // [nb][nq][nsplit][2]
   float* ws_o;             // [nb][nq][nsplit][D]
   unsigned* counters;      // [nb][nq / HPC]
@@ -47,21 +48,35 @@ struct AttnArgs {
 };
 
 template <int D, int HPC>
+__host__ __device__ inline size_t attn_smem_bytes(int nstage) {
+  return (size_t)nstage * 2 * kAttnTile * D * 2                      // K, V tiles (bf16)
+         + ((size_t)HPC * D + 2 * D + HPC * kAttnTile + 4 * HPC) * 4;  // q, new k/v, scores, stats
+}
+
+template <int D, int HPC>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
-  constexpr int PL = D / 32;        // q/k elements per lane (score phase)
+  constexpr int PL = D / 32;                                    // q/k elements per lane (scores)
   constexpr int PT = D >= kAttnThreads ? D / kAttnThreads : 1;  // output elements per thread
   static_assert(PL >= 2 && PL % 2 == 0, "head dim must be a multiple of 64");
-  __shared__ __align__(16) float qs[HPC][D];
-  __shared__ __align__(16) float knew[D];
-  __shared__ __align__(16) float vnew[D];
-  __shared__ float sc[HPC][kAttnTile];
-  __shared__ float resc[HPC];
-  __shared__ float red[32 * 2];
+  constexpr int TD = kAttnTile * D;
+  extern __shared__ __align__(16) unsigned char asmem[];
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(asmem);  // [nstage][TILE][D]
+  __nv_bfloat16* Vs = Ks + (size_t)a.nstage * TD;                // [nstage][TILE][D]
+  float* qs = reinterpret_cast<float*>(Vs + (size_t)a.nstage * TD);  // [HPC][D]
+  float* knew = qs + HPC * D;
+  float* vnew = knew + D;
+  float* sc = vnew + D;          // [HPC][TILE]
+  float* resc = sc + HPC * kAttnTile;
+  float* m_sh = resc + HPC;
+  float* l_sh = m_sh + HPC;
+
   const int split = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h0 = hg * HPC;
   const int n_hg = a.nq / HPC;
 
+  pdl_trigger();
+  pdl_wait();
   int p = a.positions[b];
   const int slot = a.slots[b];
   bool bad = false;
@@ -74,38 +89,75 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   const int j0 = lo + split * chunk;
   const int j1 = min(p + 1, j0 + chunk);
   const bool has_p = (p >= 0) && (j0 <= p) && (p < j1);
+  const int ntiles = j1 > j0 ? (j1 - j0 + kAttnTile - 1) / kAttnTile : 0;
+  const __nv_bfloat16* kbase = a.kc + (size_t)(slot < 0 ? 0 : slot) * a.t_max * D;
+  const __nv_bfloat16* vbase = a.vc + (size_t)(slot < 0 ? 0 : slot) * a.t_max * D;
+
+  // tile loader: keys [t0, t0 + 32) clipped to j1; rows past it are zero-filled
+  auto load_tile = [&](int ti) {
+    const int t0 = j0 + ti * kAttnTile;
+    const int st = ti % a.nstage;
+    constexpr int C8 = D / 8;  // 16-byte chunks per row
+    for (int i = tid; i < kAttnTile * C8; i += kAttnThreads) {
+      const int r = i / C8, c = i - r * C8;
+      const bool ok = t0 + r < j1;
+      const size_t off = (size_t)(ok ? t0 + r : 0) * D + 8 * c;
+      cp_async16(Ks + (size_t)st * TD + r * D + 8 * c, kbase + off, ok);
+      cp_async16(Vs + (size_t)st * TD + r * D + 8 * c, vbase + off, ok);
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+  if (ntiles > 0) load_tile(0);
+  if (ntiles > 1 && a.nstage > 1) load_tile(1);
 
   // ---- q: per-head RMSNorm then RoPE at position p
   const float* qraw = a.qkv + (size_t)b * a.qkv_stride;
-  if (j0 < j1) {
+  if (ntiles > 0) {
     for (int hh = warp; hh < HPC; hh += kAttnThreads / 32) {
       const float* src = qraw + (size_t)(h0 + hh) * D;
+      float qv[D / 32];
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) qv[e] = src[lane + 32 * e];
       float ss = 0.f;
-      for (int e = lane; e < D; e += 32) ss += src[e] * src[e];
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) ss += qv[e] * qv[e];
       ss = warp_sum(ss);
       const float den = rms_denom(ss, D, a.eps);
-      for (int i = lane; i < D / 2; i += 32) {
-        const float qa = (src[i] / den) * bf16f(a.g_q[i]);
-        const float qb = (src[i + D / 2] / den) * bf16f(a.g_q[i + D / 2]);
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) qs[hh * D + lane + 32 * e] = (qv[e] / den) * bf16f(a.g_q[lane + 32 * e]);
+      __syncwarp();
+#pragma unroll
+      for (int e = 0; e < D / 64; ++e) {
+        const int i = lane + 32 * e;
+        const float qa = qs[hh * D + i], qb = qs[hh * D + i + D / 2];
         const float c = a.rope_cos[(size_t)p * (D / 2) + i], s = a.rope_sin[(size_t)p * (D / 2) + i];
-        qs[hh][i] = qa * c - qb * s;
-        qs[hh][i + D / 2] = qb * c + qa * s;
+        qs[hh * D + i] = qa * c - qb * s;
+        qs[hh * D + i + D / 2] = qb * c + qa * s;
       }
     }
   }
-  // ---- new K/V row of an owning layer (position p)
-  if (a.own && has_p && warp == 0) {
+  // ---- new K/V row of an owning layer (position p), computed by every CTA holding key p
+  const bool use_new = a.own && has_p;
+  if (use_new && warp == 0) {
     const float* kr = qraw + (size_t)a.nq * D;
     const float* vr = kr + D;
+    float kv_[D / 32];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) kv_[e] = kr[lane + 32 * e];
     float ss = 0.f;
-    for (int e = lane; e < D; e += 32) ss += kr[e] * kr[e];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) ss += kv_[e] * kv_[e];
     ss = warp_sum(ss);
     const float den = rms_denom(ss, D, a.eps);
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) knew[lane + 32 * e] = (kv_[e] / den) * bf16f(a.g_k[lane + 32 * e]);
+    __syncwarp();
     __nv_bfloat16* kdst = a.kc + ((size_t)slot * a.t_max + p) * D;
     __nv_bfloat16* vdst = a.vc + ((size_t)slot * a.t_max + p) * D;
-    for (int i = lane; i < D / 2; i += 32) {
-      const float ka = (kr[i] / den) * bf16f(a.g_k[i]);
-      const float kb = (kr[i + D / 2] / den) * bf16f(a.g_k[i + D / 2]);
+#pragma unroll
+    for (int e = 0; e < D / 64; ++e) {
+      const int i = lane + 32 * e;
+      const float ka = knew[i], kb = knew[i + D / 2];
       const float c = a.rope_cos[(size_t)p * (D / 2) + i], s = a.rope_sin[(size_t)p * (D / 2) + i];
       const __nv_bfloat16 k1 = __float2bfloat16_rn(ka * c - kb * s);
       const __nv_bfloat16 k2 = __float2bfloat16_rn(kb * c + ka * s);
@@ -113,15 +165,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       knew[i + D / 2] = bf16f(k2);
       if (hg == 0) { kdst[i] = k1; kdst[i + D / 2] = k2; }
     }
-    for (int e = lane; e < D; e += 32) {
-      const __nv_bfloat16 v1 = __float2bfloat16_rn(vr[e]);
-      vnew[e] = bf16f(v1);
-      if (hg == 0) vdst[e] = v1;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      const __nv_bfloat16 v1 = __float2bfloat16_rn(vr[lane + 32 * e]);
+      vnew[lane + 32 * e] = bf16f(v1);
+      if (hg == 0) vdst[lane + 32 * e] = v1;
     }
   }
-  __syncthreads();
 
-  // ---- chunk: tiles of 32 keys, online softmax
+  // ---- tiles with online softmax
   float m_run[HPC], l_run[HPC];
   float acc[HPC][PT];
 #pragma unroll
@@ -131,106 +183,106 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 #pragma unroll
     for (int e = 0; e < PT; ++e) acc[h][e] = 0.f;
   }
-  const __nv_bfloat16* kbase = a.kc + (size_t)(slot < 0 ? 0 : slot) * a.t_max * D;
-  const __nv_bfloat16* vbase = a.vc + (size_t)(slot < 0 ? 0 : slot) * a.t_max * D;
-  const bool use_new = a.own && has_p;
-
-  for (int t0 = j0; t0 < j1; t0 += kAttnTile) {
+  for (int ti = 0; ti < ntiles; ++ti) {
+    const int t0 = j0 + ti * kAttnTile;
     const int tn = min(kAttnTile, j1 - t0);
+    const int st = ti % a.nstage;
+    if (a.nstage > 1 && ti + 1 < ntiles) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    __syncthreads();
+    const __nv_bfloat16* Kt = Ks + (size_t)st * TD;
+    const __nv_bfloat16* Vt = Vs + (size_t)st * TD;
     // scores: warp per key, lanes over D
     for (int jj = warp; jj < kAttnTile; jj += kAttnThreads / 32) {
       const int j = t0 + jj;
       float kv[PL];
-      if (jj < tn) {
-        if (use_new && j == p) {
+      if (use_new && j == p) {
 #pragma unroll
-          for (int e = 0; e < PL; ++e) kv[e] = knew[lane * PL + e];
-        } else {
-          const __nv_bfloat16* kp = kbase + (size_t)j * D + lane * PL;
-          if constexpr (PL % 8 == 0) {
+        for (int e = 0; e < PL; ++e) kv[e] = knew[lane * PL + e];
+      } else if constexpr (PL % 8 == 0) {
 #pragma unroll
-            for (int c = 0; c < PL / 8; ++c) {
-              const uint4 u = reinterpret_cast<const uint4*>(kp)[c];
-              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        for (int c = 0; c < PL / 8; ++c) {
+          const uint4 u = reinterpret_cast<const uint4*>(Kt + jj * D + lane * PL)[c];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-              for (int m = 0; m < 4; ++m) { kv[c * 8 + 2 * m] = bf16_lo(w[m]); kv[c * 8 + 2 * m + 1] = bf16_hi(w[m]); }
-            }
-          } else {
+          for (int m = 0; m < 4; ++m) { kv[c * 8 + 2 * m] = bf16_lo(w[m]); kv[c * 8 + 2 * m + 1] = bf16_hi(w[m]); }
+        }
+      } else {
 #pragma unroll
-            for (int c = 0; c < PL / 2; ++c) {
-              const uint32_t w = reinterpret_cast<const uint32_t*>(kp)[c];
-              kv[2 * c] = bf16_lo(w); kv[2 * c + 1] = bf16_hi(w);
-            }
-          }
+        for (int c = 0; c < PL / 2; ++c) {
+          const uint32_t w = reinterpret_cast<const uint32_t*>(Kt + jj * D + lane * PL)[c];
+          kv[2 * c] = bf16_lo(w);
+          kv[2 * c + 1] = bf16_hi(w);
         }
       }
 #pragma unroll
       for (int h = 0; h < HPC; ++h) {
         float d = 0.f;
-        if (jj < tn) {
 #pragma unroll
-          for (int e = 0; e < PL; ++e) d += qs[h][lane * PL + e] * kv[e];
-        }
+        for (int e = 0; e < PL; ++e) d += qs[h * D + lane * PL + e] * kv[e];
         d = warp_sum(d);
-        if (lane == 0) sc[h][jj] = (jj < tn) ? d * a.scale : -INFINITY;
+        if (lane == 0) sc[h * kAttnTile + jj] = (jj < tn) ? d * a.scale : -INFINITY;
       }
     }
     __syncthreads();
     // softmax statistics per head (warp per head)
-    for (int h = warp; h < HPC; h += kAttnThreads / 32) {
-      const float s = sc[h][lane];
+#pragma unroll
+    for (int h = 0; h < HPC; ++h) {
+      if ((h % (kAttnThreads / 32)) != warp) continue;
+      const float s = sc[h * kAttnTile + lane];
       const float mt = warp_max(s);
       const float mn = fmaxf(m_run[h], mt);
       const float pj = (lane < tn) ? expf(s - mn) : 0.f;
       const float ls = warp_sum(pj);
       const float r = expf(m_run[h] - mn);  // 0 on the first tile
-      sc[h][lane] = pj;
+      sc[h * kAttnTile + lane] = pj;
       if (lane == 0) resc[h] = r;
       m_run[h] = mn;
       l_run[h] = l_run[h] * r + ls;
     }
     __syncthreads();
     // P V: thread owns PT contiguous elements of each head's output
-#pragma unroll
-    for (int h = 0; h < HPC; ++h) {
-      const float r = resc[h];
-#pragma unroll
-      for (int e = 0; e < PT; ++e) acc[h][e] *= r;
-    }
-    for (int jj = 0; jj < tn && tid * PT < D; ++jj) {
-      const int j = t0 + jj;
-      float vv[PT];
-      if (use_new && j == p) {
-#pragma unroll
-        for (int e = 0; e < PT; ++e) vv[e] = vnew[tid * PT + e];
-      } else {
-        const __nv_bfloat16* vp = vbase + (size_t)j * D + tid * PT;
-        if constexpr (PT == 1) {
-          vv[0] = bf16f(vp[0]);
-        } else if constexpr (PT == 2) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-          vv[0] = bf16_lo(w); vv[1] = bf16_hi(w);
-        } else if constexpr (PT == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(vp);
-          vv[0] = bf16_lo(w.x); vv[1] = bf16_hi(w.x); vv[2] = bf16_lo(w.y); vv[3] = bf16_hi(w.y);
-        } else {
-#pragma unroll
-          for (int e = 0; e < PT; ++e) vv[e] = bf16f(vp[e]);
-        }
-      }
+    if (tid * PT < D) {
 #pragma unroll
       for (int h = 0; h < HPC; ++h) {
-        const float pj = sc[h][jj];
+        const float r = resc[h];
 #pragma unroll
-        for (int e = 0; e < PT; ++e) acc[h][e] += pj * vv[e];
+        for (int e = 0; e < PT; ++e) acc[h][e] *= r;
+      }
+      for (int jj = 0; jj < tn; ++jj) {
+        const int j = t0 + jj;
+        float vv[PT];
+        if (use_new && j == p) {
+#pragma unroll
+          for (int e = 0; e < PT; ++e) vv[e] = vnew[tid * PT + e];
+        } else {
+          const __nv_bfloat16* vp = Vt + jj * D + tid * PT;
+          if constexpr (PT == 1) {
+            vv[0] = bf16f(vp[0]);
+          } else if constexpr (PT == 2) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
+            vv[0] = bf16_lo(w);
+            vv[1] = bf16_hi(w);
+          } else {
+            const uint2 w = *reinterpret_cast<const uint2*>(vp);
+            vv[0] = bf16_lo(w.x); vv[1] = bf16_hi(w.x); vv[2] = bf16_lo(w.y); vv[3] = bf16_hi(w.y);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) {
+          const float pj = sc[h * kAttnTile + jj];
+#pragma unroll
+          for (int e = 0; e < PT; ++e) acc[h][e] += pj * vv[e];
+        }
       }
     }
     __syncthreads();
+    if (a.nstage > 1 && ti + 2 < ntiles) load_tile(ti + 2);
+    else if (a.nstage == 1 && ti + 1 < ntiles) load_tile(ti + 1);
   }
-  // m_run/l_run live in the stats warps; publish them through smem.
-  __shared__ float m_sh[HPC], l_sh[HPC];
-  for (int h = warp; h < HPC; h += kAttnThreads / 32)
-    if (lane == 0) { m_sh[h] = m_run[h]; l_sh[h] = l_run[h]; }
+#pragma unroll
+  for (int h = 0; h < HPC; ++h)
+    if ((h % (kAttnThreads / 32)) == warp && lane == 0) { m_sh[h] = m_run[h]; l_sh[h] = l_run[h]; }
   __syncthreads();
 
   float* outb = a.out + (size_t)b * a.out_stride;
@@ -263,27 +315,51 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  for (int h = 0; h < HPC && tid * PT < D; ++h) {
+  // merge: w_s = exp(m_s - M) per split (empty splits carry l = 0 and o = 0), then
+  // o = sum_s w_s o_s / sum_s w_s l_s
+  __shared__ float wgt[64];
+  for (int h = 0; h < HPC; ++h) {
     const size_t row0 = base_ml + (size_t)(h0 + h) * a.nsplit;
-    float M = -INFINITY;
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float l = ldcg(a.ws_ml + (row0 + s) * 2 + 1);
-      if (l > 0.f) M = fmaxf(M, ldcg(a.ws_ml + (row0 + s) * 2));
+    if (warp == 0) {
+      float mv[2], lv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int s = lane + 32 * u;
+        mv[u] = -INFINITY;
+        lv[u] = 0.f;
+        if (s < a.nsplit) { mv[u] = ldcg(a.ws_ml + (row0 + s) * 2); lv[u] = ldcg(a.ws_ml + (row0 + s) * 2 + 1); }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) if (lv[u] > 0.f) M = fmaxf(M, mv[u]);
+      M = warp_max(M);
+      float L = 0.f;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int s = lane + 32 * u;
+        const float w = (lv[u] > 0.f) ? expf(mv[u] - M) : 0.f;
+        if (s < a.nsplit) wgt[s] = w;
+        L += w * lv[u];
+      }
+      L = warp_sum(L);
+      if (lane == 0) l_sh[h] = L;
     }
-    float L = 0.f;
-    float o[PT];
+    __syncthreads();
+    const float L = l_sh[h];
+    if (tid * PT < D) {
+      float o[PT];
 #pragma unroll
-    for (int e = 0; e < PT; ++e) o[e] = 0.f;
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float l = ldcg(a.ws_ml + (row0 + s) * 2 + 1);
-      if (!(l > 0.f)) continue;
-      const float w = expf(ldcg(a.ws_ml + (row0 + s) * 2) - M);
-      L += w * l;
+      for (int e = 0; e < PT; ++e) o[e] = 0.f;
+#pragma unroll 4
+      for (int s = 0; s < a.nsplit; ++s) {
+        const float w = wgt[s];
 #pragma unroll
-      for (int e = 0; e < PT; ++e) o[e] += w * ldcg(a.ws_o + (row0 + s) * D + tid * PT + e);
+        for (int e = 0; e < PT; ++e) o[e] += w * ldcg(a.ws_o + (row0 + s) * D + tid * PT + e);
+      }
+#pragma unroll
+      for (int e = 0; e < PT; ++e) outb[(h0 + h) * D + tid * PT + e] = L > 0.f ? o[e] / L : 0.f;
     }
-#pragma unroll
-    for (int e = 0; e < PT; ++e) outb[(h0 + h) * D + tid * PT + e] = L > 0.f ? o[e] / L : 0.f;
+    __syncthreads();
   }
   if (tid == 0) a.counters[b * n_hg + hg] = 0u;
 }

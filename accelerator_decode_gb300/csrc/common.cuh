@@ -90,4 +90,19 @@ __device__ __forceinline__ void set_err(int* err, int bit) {
 // Loads that bypass L1 (data written by other CTAs of the same grid).
 __device__ __forceinline__ float ldcg(const float* p) { return __ldcg(p); }
 
+// 16-byte global -> shared async copy; with pred == false the 16 bytes are zero-filled and
+// nothing is read (src must still be a valid address).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  const int sz = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(sz) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Programmatic dependent launch.  Before pdl_wait() a kernel may only read data that no
+// kernel of the step writes (weights, RoPE tables); every global write and every read of an
+// activation comes after it.  Both are no-ops for a launch without the PDL attribute.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 }  // namespace g4

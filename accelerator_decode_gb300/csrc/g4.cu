@@ -252,22 +252,101 @@ struct Scratch {
   int* am_idx;
 };
 
-template <int FMT, int R, int EPI, int NB>
-void launch_nb(const GemvArgs& a, int grid, size_t smem, cudaStream_t st) {
-  auto k = gemv_kernel<FMT, R, NB, EPI>;
-  if (smem > 48 * 1024) cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  k<<<grid, kGemvThreads, smem, st>>>(a);
+// Programmatic dependent launch for every kernel of the step (G4_PDL=0 disables it).
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("G4_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+template <typename... KArgs, typename... Args>
+void launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Opt every kernel into the full shared-memory carve-out once per process (never during a
+// stream capture).
+template <typename... KArgs>
+void set_max_dyn(void (*k)(KArgs...), int optin) {
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+}
+template <int FMT, int R, int EPI>
+void attrs_gemv(int optin) {
+  set_max_dyn(gemv_kernel<FMT, R, 1, EPI>, optin);
+  set_max_dyn(gemv_kernel<FMT, R, 2, EPI>, optin);
+  set_max_dyn(gemv_kernel<FMT, R, 4, EPI>, optin);
+}
+template <int D>
+void attrs_attn(int optin) {
+  set_max_dyn(attn_kernel<D, 1>, optin);
+  set_max_dyn(attn_kernel<D, 2>, optin);
+  set_max_dyn(attn_kernel<D, 4>, optin);
+  set_max_dyn(attn_kernel<D, 8>, optin);
+}
+std::mutex g_attr_mu;
+std::map<int, int> g_optin;  // device -> opt-in shared memory bytes
+int init_kernel_attrs(int device) {
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  auto it = g_optin.find(device);
+  if (it != g_optin.end()) return it->second;
+  int optin = 48 * 1024;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  attrs_gemv<FMT_W4A16, 1, EPI_STORE>(optin);
+  attrs_gemv<FMT_BF16, 1, EPI_STORE>(optin);
+  attrs_gemv<FMT_W4A16, 2, EPI_GEGLU>(optin);
+  attrs_gemv<FMT_BF16, 2, EPI_GEGLU>(optin);
+  attrs_gemv<FMT_W4A16, 1, EPI_PLE>(optin);
+  attrs_gemv<FMT_BF16, 1, EPI_PLE>(optin);
+  attrs_gemv<FMT_BF16, 1, EPI_ARGMAX>(optin);
+  attrs_attn<64>(optin);
+  attrs_attn<128>(optin);
+  attrs_attn<256>(optin);
+  attrs_attn<512>(optin);
+  cudaGetLastError();
+  g_optin[device] = optin;
+  return optin;
 }
 
 template <int FMT, int R, int EPI>
-void launch_fmt(const GemvArgs& a, int nb, int grid, int sg_per_cta, cudaStream_t st) {
-  if (nb == 1) launch_nb<FMT, R, EPI, 1>(a, grid, gemv_smem_bytes<FMT, R, 1>(sg_per_cta), st);
-  else if (nb == 2) launch_nb<FMT, R, EPI, 2>(a, grid, gemv_smem_bytes<FMT, R, 2>(sg_per_cta), st);
-  else launch_nb<FMT, R, EPI, 4>(a, grid, gemv_smem_bytes<FMT, R, 4>(sg_per_cta), st);
+void launch_fmt(const GemvArgs& a, int nb, int grid, cudaStream_t st) {
+  const int kc = a.sg_per_cta * Fmt<FMT>::SGK;
+  if (nb == 1) {
+    const size_t sm = gemv_smem_plan(1, R, kc, a.pro, a.norm_n, a.ksplit).total_floats * 4;
+    launch(gemv_kernel<FMT, R, 1, EPI>, dim3(grid), dim3(kGemvThreads), sm, st, a);
+  } else if (nb == 2) {
+    const size_t sm = gemv_smem_plan(2, R, kc, a.pro, a.norm_n, a.ksplit).total_floats * 4;
+    launch(gemv_kernel<FMT, R, 2, EPI>, dim3(grid), dim3(kGemvThreads), sm, st, a);
+  } else {
+    const size_t sm = gemv_smem_plan(4, R, kc, a.pro, a.norm_n, a.ksplit).total_floats * 4;
+    launch(gemv_kernel<FMT, R, 4, EPI>, dim3(grid), dim3(kGemvThreads), sm, st, a);
+  }
+}
+
+// Grid of one GEMV launch: every (row group, K slice) when split; otherwise persistent CTAs
+// (at most 4 per SM) looping over row groups.
+int gemv_grid(const Lin& L, int sms) {
+  const int n_rg = L.n_rb / L.R;
+  if (L.ksplit > 1) return n_rg * L.ksplit;
+  return std::min(n_rg, 4 * sms);
 }
 
 // y = W x for n rows, in chunks of kMaxNB rows.
-void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const Scratch& s, cudaStream_t st) {
+void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const Scratch& s, int sms,
+              cudaStream_t st) {
   for (int b0 = 0; b0 < n; b0 += kMaxNB) {
     const int nb = std::min(kMaxNB, n - b0);
     GemvArgs a{};
@@ -303,23 +382,23 @@ void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const S
     a.next_ids = io.next_ids ? io.next_ids + b0 : nullptr;
     a.part = s.part;
     a.counters = s.cnt;
-    const int grid = (L.n_rb / L.R) * L.ksplit;
+    const int grid = gemv_grid(L, sms);
     const bool w4 = L.fmt == G4_W4A16;
     switch (epi) {
       case EPI_STORE:
-        if (w4) launch_fmt<FMT_W4A16, 1, EPI_STORE>(a, nb, grid, L.sg_per_cta, st);
-        else launch_fmt<FMT_BF16, 1, EPI_STORE>(a, nb, grid, L.sg_per_cta, st);
+        if (w4) launch_fmt<FMT_W4A16, 1, EPI_STORE>(a, nb, grid, st);
+        else launch_fmt<FMT_BF16, 1, EPI_STORE>(a, nb, grid, st);
         break;
       case EPI_GEGLU:
-        if (w4) launch_fmt<FMT_W4A16, 2, EPI_GEGLU>(a, nb, grid, L.sg_per_cta, st);
-        else launch_fmt<FMT_BF16, 2, EPI_GEGLU>(a, nb, grid, L.sg_per_cta, st);
+        if (w4) launch_fmt<FMT_W4A16, 2, EPI_GEGLU>(a, nb, grid, st);
+        else launch_fmt<FMT_BF16, 2, EPI_GEGLU>(a, nb, grid, st);
         break;
       case EPI_PLE:
-        if (w4) launch_fmt<FMT_W4A16, 1, EPI_PLE>(a, nb, grid, L.sg_per_cta, st);
-        else launch_fmt<FMT_BF16, 1, EPI_PLE>(a, nb, grid, L.sg_per_cta, st);
+        if (w4) launch_fmt<FMT_W4A16, 1, EPI_PLE>(a, nb, grid, st);
+        else launch_fmt<FMT_BF16, 1, EPI_PLE>(a, nb, grid, st);
         break;
       case EPI_ARGMAX:
-        launch_fmt<FMT_BF16, 1, EPI_ARGMAX>(a, nb, grid, L.sg_per_cta, st);
+        launch_fmt<FMT_BF16, 1, EPI_ARGMAX>(a, nb, grid, st);
         break;
     }
   }
@@ -329,7 +408,7 @@ void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const S
 template <int D, int HPC>
 void launch_attn(const AttnArgs& a, int nb, cudaStream_t st) {
   dim3 grid(a.nsplit, a.nq / HPC, nb);
-  attn_kernel<D, HPC><<<grid, kAttnThreads, 0, st>>>(a);
+  launch(attn_kernel<D, HPC>, grid, dim3(kAttnThreads), attn_smem_bytes<D, HPC>(a.nstage), st, a);
 }
 template <int D>
 void launch_attn_d(const AttnArgs& a, int hpc, int nb, cudaStream_t st) {
@@ -394,7 +473,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
                (float)std::sqrt((double)H), (float)std::sqrt((double)P), h->x0, h->tok, h->err};
   {
     ProfScope ps(prof, "embed", (double)n * (H + LP) * 2);
-    embed_kernel<<<n, 256, 0, st>>>(ea);
+    launch(embed_kernel, dim3(cdiv(H + LP, 8 * 256), n), dim3(256), 0, st, ea);
   }
   {
     ProfScope ps(prof, "gemv.ple_model_proj", (double)h->pmp.bytes);
@@ -404,12 +483,13 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
     io.x_stride = H;
     io.y = h->pr;
     io.y_stride = LP;
-    run_gemv(h->pmp, EPI_STORE, io, n, eps, s, st);
+    run_gemv(h->pmp, EPI_STORE, io, n, eps, s, h->sms, st);
   }
   {
     ProfScope ps(prof, "ple_combine", 0.0);
-    ple_combine_kernel<<<dim3(L, n), std::min(256, std::max(32, P)), 0, st>>>(
-        h->pr, h->tok, h->g_ppn, L, P, (float)(1.0 / std::sqrt((double)H)), (float)(1.0 / std::sqrt(2.0)), eps, h->ple);
+    launch(ple_combine_kernel, dim3(L, n), dim3(std::min(256, std::max(32, P))), 0, st, (const float*)h->pr,
+           (const float*)h->tok, h->g_ppn, L, P, (float)(1.0 / std::sqrt((double)H)), (float)(1.0 / std::sqrt(2.0)),
+           eps, h->ple);
   }
 
   float* cur = h->x0;
@@ -439,7 +519,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y_stride = Y.qkv.n_valid;
       {
         ProfScope ps(prof, "gemv.qkv", (double)Y.qkv.bytes);
-        run_gemv(Y.qkv, EPI_STORE, io, n, eps, s, st);
+        run_gemv(Y.qkv, EPI_STORE, io, n, eps, s, h->sms, st);
       }
       if (l > 0) {
         cur = io.x_out;
@@ -472,7 +552,9 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.out = h->attn;
       a.out_stride = nqd;
       const int hpc = attn_hpc(c.num_q_heads, n);
-      a.nsplit = attn_nsplit(h->sms, c.num_q_heads, hpc, n, Y.full ? c.max_context : std::min(c.sliding_window, c.max_context));
+      const int max_keys = Y.full ? c.max_context : std::min(c.sliding_window, c.max_context);
+      a.nsplit = attn_nsplit(h->sms, c.num_q_heads, hpc, n, max_keys);
+      a.nstage = cdiv(max_keys, a.nsplit) > kAttnTile ? 2 : 1;
       a.ws_ml = h->attn_ml;
       a.ws_o = h->attn_o;
       a.counters = h->attn_cnt;
@@ -497,7 +579,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y = h->r_attn;
       io.y_stride = H;
       ProfScope ps(prof, "gemv.o", (double)Y.o.bytes);
-      run_gemv(Y.o, EPI_STORE, io, n, eps, s, st);
+      run_gemv(Y.o, EPI_STORE, io, n, eps, s, h->sms, st);
     }
     {  // gate/up
       GemvIO io;
@@ -515,7 +597,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y_stride = Y.F;
       {
         ProfScope ps(prof, "gemv.gate_up", (double)Y.gu.bytes);
-        run_gemv(Y.gu, EPI_GEGLU, io, n, eps, s, st);
+        run_gemv(Y.gu, EPI_GEGLU, io, n, eps, s, h->sms, st);
       }
       cur = io.x_out;
     }
@@ -527,7 +609,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y = h->r_mlp;
       io.y_stride = H;
       ProfScope ps(prof, "gemv.down", (double)Y.down.bytes);
-      run_gemv(Y.down, EPI_STORE, io, n, eps, s, st);
+      run_gemv(Y.down, EPI_STORE, io, n, eps, s, h->sms, st);
     }
     {  // PLE gate
       GemvIO io;
@@ -547,7 +629,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.ple_stride = LP;
       {
         ProfScope ps(prof, "gemv.ple_gate", (double)Y.pg.bytes);
-        run_gemv(Y.pg, EPI_PLE, io, n, eps, s, st);
+        run_gemv(Y.pg, EPI_PLE, io, n, eps, s, h->sms, st);
       }
       cur = io.x_out;
     }
@@ -559,7 +641,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y = h->r_ple;
       io.y_stride = H;
       ProfScope ps(prof, "gemv.ple_proj", (double)Y.pp.bytes);
-      run_gemv(Y.pp, EPI_STORE, io, n, eps, s, st);
+      run_gemv(Y.pp, EPI_STORE, io, n, eps, s, h->sms, st);
     }
   }
   {  // final norm, lm_head, argmax
@@ -580,7 +662,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
     io.next_ids = d_next;
     {
       ProfScope ps(prof, "gemv.lm_head_argmax", (double)h->lm.bytes);
-      run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, st);
+      run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, h->sms, st);
     }
     if (h->trace)
       for (int i = 0; i < n; ++i)
@@ -605,7 +687,7 @@ g4_status validate(const g4_config* c) {
   if (c->num_kv_heads != 1 || c->group_size != 32) return G4_ERR_UNSUPPORTED;
   if (!is_pow2_dim(c->head_dim_sliding) || !is_pow2_dim(c->head_dim_full)) return G4_ERR_UNSUPPORTED;
   if (c->hidden % 32 || c->mlp % 32 || c->mlp_shared % 32 || c->ple_dim % 32) return G4_ERR_UNSUPPORTED;
-  if (c->max_batch > 64 || c->ple_dim > 1024) return G4_ERR_UNSUPPORTED;
+  if (c->max_batch > 64 || c->ple_dim > 1024 || c->hidden > 8192) return G4_ERR_UNSUPPORTED;
   return G4_OK;
 }
 
@@ -805,6 +887,7 @@ g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
   if (v != G4_OK) return v;
   if (!weights) return G4_ERR_INVALID_ARG;
   CK(cudaSetDevice(device));
+  init_kernel_attrs(device);
   g4_handle* h = new g4_handle();
   h->cfg = *cfg;
   h->device = device;
@@ -999,6 +1082,7 @@ g4_status g4_linear_create(int device, int32_t weight_format, int32_t n_out, int
   if (weight_format == G4_W4A16 && !d_scales) return G4_ERR_INVALID_ARG;
   *out = nullptr;
   CK(cudaSetDevice(device));
+  init_kernel_attrs(device);
   g4_linear_op* op = new g4_linear_op();
   op->h.device = device;
   cudaDeviceGetAttribute(&op->h.sms, cudaDevAttrMultiProcessorCount, device);
@@ -1035,7 +1119,7 @@ g4_status g4_linear_forward(g4_linear_op* op, g4_stream stream, int32_t n_rows, 
   io.y = d_y;
   io.y_stride = op->lin.n_valid;
   Scratch s{op->h.gemv_part, op->h.gemv_cnt, nullptr, nullptr};
-  run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, reinterpret_cast<cudaStream_t>(stream));
+  run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, op->h.sms, reinterpret_cast<cudaStream_t>(stream));
   CK(cudaGetLastError());
   return G4_OK;
 }

@@ -17,10 +17,12 @@
 // work; "Gemma 4 E2B in Pure JAX on a Colab TPU", cell 1.2).  Accumulation is fp32 (packed
 // fp32x2 FMA) with fp32 activations.
 //
-// CTA = 4 warps on one row group (R row blocks); warps take different supergroups of the
-// CTA's K chunk; a K split over CTAs is reduced by the last CTA to finish, summing the
-// partials in split order (deterministic).  The prologue (norm / residual update) is
-// recomputed by every CTA from the full input vector; block 0 writes the new residual.
+// Work: CTA = 4 warps on one row group (R row blocks) and one K slice; warps take different
+// supergroups of the slice.  With one K slice, CTAs loop over row groups (persistent) and
+// prefetch the next row group's weights before reducing the current one; with several, the
+// last CTA of a row group sums the slices' partials in slice order (deterministic).
+// Latency: the first weights are requested before griddepcontrol.wait (programmatic
+// dependent launch), and the activation rows are staged with one wave of cp.async.
 #pragma once
 #include "common.cuh"
 
@@ -43,8 +45,8 @@ struct GemvArgs {
   int S;          // supergroups along K
   int tiles;      // tiles per row = 8 * S
   int nb;         // batch rows in this launch (<= kMaxNB)
-  int ksplit;     // CTAs along K per row group
-  int sg_per_cta; // supergroups per CTA
+  int ksplit;     // K slices (CTAs along K per row group)
+  int sg_per_cta; // supergroups per slice
   // prologue
   int pro;
   const float* x_in;
@@ -77,6 +79,24 @@ struct Fmt {
   static constexpr int SGK = FMT == FMT_W4A16 ? 256 : 64;  // k per supergroup
   static constexpr int TK = SGK / 8;                        // k per tile
 };
+
+// Shared-memory plan (floats), identical on host and device.
+struct GemvSmem {
+  int xs, red, stage, gath, total_floats;
+};
+__host__ __device__ inline GemvSmem gemv_smem_plan(int NB, int R, int kc, int pro, int n, int ksplit) {
+  GemvSmem p;
+  const int nv = R * NB * 32;
+  int red = (kGemvWarps + 1) * nv;
+  if (red < 32 * NB) red = 32 * NB;
+  p.xs = 0;
+  p.red = NB * kc;
+  p.stage = p.red + red;
+  const int stage = pro == PRO_PLAIN ? 0 : 2 * NB * n + n;  // x rows, r rows, two bf16 gain vectors
+  p.gath = p.stage + stage;
+  p.total_floats = p.gath + (ksplit > 1 ? nv * ksplit : 0);
+  return p;
+}
 
 // Accumulate one tile (one row, TK k values) into acc[b] for NB activation rows.
 template <int FMT, int NB>
@@ -132,74 +152,91 @@ __device__ __forceinline__ void tile_fma(const uint4 wv, uint32_t s2, const floa
   }
 }
 
-// Prologue: stage the activation chunk [k0, k1) of NB rows into smem (fp32), zero-padded.
+// Prologue: stage the activation chunk [k0, k0 + kc) of NB rows into xs (fp32), zero-padded
+// beyond k1 and beyond nb.  PRO_NORM / PRO_RESID first stage whole rows (one cp.async wave),
+// then reduce from shared memory.
 template <int NB>
-__device__ __forceinline__ void gemv_prologue(const GemvArgs& a, float* xs, int kc, int k0, int k1,
-                                              float* red) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ void gemv_prologue(const GemvArgs& a, float* smem, const GemvSmem& L, int kc, int k0,
+                                              int k1) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  float* xs = smem + L.xs;
+  float* red = smem + L.red;
   if (a.pro == PRO_PLAIN) {
-    for (int b = 0; b < NB; ++b) {
-      for (int k = k0 + tid; k < k0 + kc; k += blockDim.x)
-        xs[b * kc + (k - k0)] = (b < a.nb && k < k1) ? a.x_in[b * a.x_stride + k] : 0.f;
+    const int c4 = kc / 4;
+    for (int i = tid; i < NB * c4; i += nt) {
+      const int b = i / c4, c = i - b * c4, k = k0 + 4 * c;
+      const bool ok = b < a.nb && k < k1;
+      cp_async16(xs + b * kc + 4 * c, ok ? a.x_in + (size_t)b * a.x_stride + k : a.x_in, ok);
     }
+    cp_async_wait_all();
+    __syncthreads();
     return;
   }
   const int n = a.norm_n;
-  float rd[NB];  // denominators of r (PRO_RESID)
-  if (a.pro == PRO_RESID) {
+  float* xin = smem + L.stage;
+  float* rin = xin + NB * n;
+  __nv_bfloat16* gr = reinterpret_cast<__nv_bfloat16*>(rin + NB * n);
+  __nv_bfloat16* ga = gr + n;
+  const bool resid = a.pro == PRO_RESID;
+  const int c4 = n / 4;
+  for (int i = tid; i < NB * c4; i += nt) {
+    const int b = i / c4, c = i - b * c4;
+    const bool ok = b < a.nb;
+    cp_async16(xin + b * n + 4 * c, ok ? a.x_in + (size_t)b * a.x_stride + 4 * c : a.x_in, ok);
+    if (resid) cp_async16(rin + b * n + 4 * c, ok ? a.r_in + (size_t)b * a.r_stride + 4 * c : a.r_in, ok);
+  }
+  for (int i = tid; i < n / 8; i += nt) {
+    if (resid) cp_async16(gr + 8 * i, a.g_r + 8 * i, true);
+    if (a.g_a) cp_async16(ga + 8 * i, a.g_a + 8 * i, true);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  if (resid) {
     float ss[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
       ss[b] = 0.f;
-      if (b < a.nb)
-        for (int k = tid; k < n; k += blockDim.x) {
-          float v = a.r_in[b * a.r_stride + k];
-          ss[b] += v * v;
-        }
+      for (int k = tid; k < n; k += nt) ss[b] += rin[b * n + k] * rin[b * n + k];
     }
     block_sum<NB>(ss, red);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) rd[b] = rms_denom(ss[b], n, a.eps);
-  }
-  // New residual value at k (PRO_RESID), or the input itself (PRO_NORM).
-  auto xval = [&](int b, int k) -> float {
-    float x = a.x_in[b * a.x_stride + k];
-    if (a.pro == PRO_RESID) {
-      float r = a.r_in[b * a.r_stride + k];
-      x = (x + (r / rd[b]) * bf16f(a.g_r[k])) * a.lambda;
+    for (int b = 0; b < NB; ++b) {
+      const float rd = rms_denom(ss[b], n, a.eps);
+      for (int k = tid; k < n; k += nt)
+        xin[b * n + k] = (xin[b * n + k] + (rin[b * n + k] / rd) * bf16f(gr[k])) * a.lambda;
     }
-    return x;
-  };
-  if (a.pro == PRO_RESID && blockIdx.x == 0) {
-    for (int b = 0; b < a.nb; ++b)
-      for (int k = tid; k < n; k += blockDim.x) a.x_out[b * a.x_stride + k] = xval(b, k);
+    __syncthreads();
+    if (blockIdx.x == 0) {
+      for (int i = tid; i < a.nb * c4; i += nt) {
+        const int b = i / c4, c = i - b * c4;
+        *reinterpret_cast<float4*>(a.x_out + (size_t)b * a.x_stride + 4 * c) =
+            *reinterpret_cast<const float4*>(xin + b * n + 4 * c);
+      }
+    }
   }
   float ad[NB];
   if (a.g_a != nullptr) {
-    float ss[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      ss[b] = 0.f;
-      if (b < a.nb)
-        for (int k = tid; k < n; k += blockDim.x) {
-          float v = xval(b, k);
-          ss[b] += v * v;
-        }
+      ad[b] = 0.f;
+      for (int k = tid; k < n; k += nt) ad[b] += xin[b * n + k] * xin[b * n + k];
     }
-    block_sum<NB>(ss, red);
+    block_sum<NB>(ad, red);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) ad[b] = rms_denom(ss[b], n, a.eps);
+    for (int b = 0; b < NB; ++b) ad[b] = rms_denom(ad[b], n, a.eps);
   }
+#pragma unroll
   for (int b = 0; b < NB; ++b) {
-    for (int k = k0 + tid; k < k0 + kc; k += blockDim.x) {
+    for (int k = k0 + tid; k < k0 + kc; k += nt) {
       float v = 0.f;
       if (b < a.nb && k < k1) {
-        v = xval(b, k);
-        if (a.g_a != nullptr) v = (v / ad[b]) * bf16f(a.g_a[k]);
+        v = xin[b * n + k];
+        if (a.g_a != nullptr) v = (v / ad[b]) * bf16f(ga[k]);
       }
       xs[b * kc + (k - k0)] = v;
     }
   }
+  __syncthreads();
 }
 
 template <int FMT, int R, int NB, int EPI>
@@ -207,132 +244,162 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
   using F = Fmt<FMT>;
   extern __shared__ __align__(16) float smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rg = blockIdx.x / a.ksplit, ks = blockIdx.x % a.ksplit;
+  const int ks = blockIdx.x % a.ksplit;
+  const int rg_step = gridDim.x / a.ksplit;
+  const int n_rg = a.n_rb / R;
   const int sg0 = ks * a.sg_per_cta;
   const int sg1 = min(a.S, sg0 + a.sg_per_cta);
-  const int kc = a.sg_per_cta * F::SGK;          // smem chunk width
+  const int kc = a.sg_per_cta * F::SGK;
   const int k0 = sg0 * F::SGK;
   const int k1 = min(a.K, sg1 * F::SGK);
-  float* xs = smem;                               // [NB][kc]
-  float* red = smem + NB * kc;                    // [kGemvWarps][R*NB*32] (also block_sum)
-
-  // Issue this warp's first supergroup of weights before the prologue: weights never
-  // depend on activations.
+  const GemvSmem L = gemv_smem_plan(NB, R, kc, a.pro, a.norm_n, a.ksplit);
   const int rows_total = a.n_rb * 32;
-  int sg = sg0 + warp;
+  const int sg_first = sg0 + warp;
+
+  pdl_trigger();
   uint4 wbuf[R][8];
   uint4 sbuf[R];
-  auto load_sg = [&](int s) {
+  auto load_sg = [&](int rg_, int s) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const int rb = rg * R + r;
+      const int rb = rg_ * R + r;
       const uint4* base = a.qw + ((size_t)rb * a.tiles + (size_t)s * 8) * 32 + lane;
 #pragma unroll
       for (int t = 0; t < 8; ++t) wbuf[r][t] = __ldg(base + t * 32);
       if constexpr (FMT == FMT_W4A16) sbuf[r] = __ldg(a.sc + ((size_t)rb * a.S + s) * 32 + lane);
     }
   };
-  if (sg < sg1) load_sg(sg);
+  int rg = blockIdx.x / a.ksplit;
+  if (rg < n_rg && sg_first < sg1) load_sg(rg, sg_first);  // weights never depend on activations
+  pdl_wait();
+  gemv_prologue<NB>(a, smem, L, kc, k0, k1);
 
-  gemv_prologue<NB>(a, xs, kc, k0, k1, red);
-  __syncthreads();
-
-  float2 acc[R][NB];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
-
-  while (sg < sg1) {
-    const float* xsg = xs + (sg - sg0) * F::SGK;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        uint32_t s2 = 0;
-        if constexpr (FMT == FMT_W4A16) {
-          const uint32_t sw = (&sbuf[r].x)[t >> 1];
-          const uint32_t h = (t & 1) ? (sw >> 16) : (sw & 0xFFFFu);
-          s2 = h | (h << 16);
-        }
-        tile_fma<FMT, NB>(wbuf[r][t], s2, xsg + t * F::TK, kc, acc[r]);
-      }
-    }
-    sg += kGemvWarps;
-    if (sg < sg1) load_sg(sg);
-  }
-
-  // Cross-warp reduction in fixed warp order.
+  float* xs = smem + L.xs;
+  float* red = smem + L.red;
   constexpr int NV = R * NB * 32;
-  float* wred = red;  // [kGemvWarps][NV]
-  __syncthreads();
+  float* fin = red + kGemvWarps * NV;
+  float best_v[NB];
+  int best_i[NB];
 #pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int b = 0; b < NB; ++b) wred[warp * NV + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
-  __syncthreads();
-  float* fin = red + kGemvWarps * NV;  // [NV]
-  for (int i = threadIdx.x; i < NV; i += blockDim.x) {
-    float s = 0.f;
-#pragma unroll
-    for (int w = 0; w < kGemvWarps; ++w) s += wred[w * NV + i];
-    fin[i] = s;
-  }
-  __syncthreads();
+  for (int b = 0; b < NB; ++b) { best_v[b] = __int_as_float(0x7fc00000); best_i[b] = 0x7fffffff; }
 
-  if (a.ksplit > 1) {
-    // partial -> scratch; the last CTA of the row group sums all partials in split order.
-    for (int i = threadIdx.x; i < NV; i += blockDim.x) {
-      const int b = (i / 32) % NB, r = i / (32 * NB), l = i % 32;
-      if (b < a.nb) a.part[((size_t)ks * a.nb + b) * rows_total + (rg * R + r) * 32 + l] = fin[i];
+  for (; rg < n_rg; rg += rg_step) {
+    float2 acc[R][NB];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+    int sg = sg_first;
+    while (sg < sg1) {
+      const float* xsg = xs + (sg - sg0) * F::SGK;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          uint32_t s2 = 0;
+          if constexpr (FMT == FMT_W4A16) {
+            const uint32_t sw = (&sbuf[r].x)[t >> 1];
+            const uint32_t hh = (t & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+            s2 = hh | (hh << 16);
+          }
+          tile_fma<FMT, NB>(wbuf[r][t], s2, xsg + t * F::TK, kc, acc[r]);
+        }
+      }
+      sg += kGemvWarps;
+      if (sg < sg1) load_sg(rg, sg);
+      else if (rg + rg_step < n_rg && sg_first < sg1) load_sg(rg + rg_step, sg_first);  // next row group
     }
-    __threadfence();
+
+    // cross-warp reduction in fixed warp order
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) red[warp * NV + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
     __syncthreads();
-    __shared__ int is_last;
-    if (threadIdx.x == 0) {
-      unsigned prev = atomicAdd(&a.counters[rg], 1u);
-      is_last = (prev == (unsigned)a.ksplit - 1);
-    }
-    __syncthreads();
-    if (!is_last) return;
-    __threadfence();
     for (int i = threadIdx.x; i < NV; i += blockDim.x) {
-      const int b = (i / 32) % NB, r = i / (32 * NB), l = i % 32;
       float s = 0.f;
-      if (b < a.nb)
-        for (int q = 0; q < a.ksplit; ++q)
-          s += ldcg(a.part + ((size_t)q * a.nb + b) * rows_total + (rg * R + r) * 32 + l);
+#pragma unroll
+      for (int w = 0; w < kGemvWarps; ++w) s += red[w * NV + i];
       fin[i] = s;
     }
-    if (threadIdx.x == 0) a.counters[rg] = 0u;
     __syncthreads();
-  }
 
-  // Epilogue (threads of warp 0 own lanes).
-  if constexpr (EPI == EPI_ARGMAX) {
-    __shared__ float bv[kMaxNB];
-    __shared__ int bi[kMaxNB];
+    if (a.ksplit > 1) {  // one row group per CTA here (grid = n_rg * ksplit)
+      for (int i = threadIdx.x; i < NV; i += blockDim.x) {
+        const int b = (i / 32) % NB, r = i / (32 * NB), l = i % 32;
+        if (b < a.nb) a.part[((size_t)ks * a.nb + b) * rows_total + (rg * R + r) * 32 + l] = fin[i];
+      }
+      __threadfence();
+      __syncthreads();
+      __shared__ int is_last;
+      if (threadIdx.x == 0) is_last = atomicAdd(&a.counters[rg], 1u) == (unsigned)a.ksplit - 1;
+      __syncthreads();
+      if (!is_last) return;
+      __threadfence();
+      float* gath = smem + L.gath;  // [ksplit][NV]
+      for (int i = threadIdx.x; i < NV * a.ksplit; i += blockDim.x) {
+        const int q = i / NV, v = i - q * NV;
+        const int b = (v / 32) % NB, r = v / (32 * NB), l = v % 32;
+        gath[i] = b < a.nb ? ldcg(a.part + ((size_t)q * a.nb + b) * rows_total + (rg * R + r) * 32 + l) : 0.f;
+      }
+      __syncthreads();
+      for (int i = threadIdx.x; i < NV; i += blockDim.x) {
+        float s = 0.f;
+        for (int q = 0; q < a.ksplit; ++q) s += gath[q * NV + i];
+        fin[i] = s;
+      }
+      if (threadIdx.x == 0) a.counters[rg] = 0u;
+      __syncthreads();
+    }
+
     if (warp == 0) {
       for (int b = 0; b < a.nb; ++b) {
-        const int n = rg * 32 + lane;
-        float v = fin[b * 32 + lane];
-        int idx = n;
-        if (n >= a.n_valid) { v = __int_as_float(0x7fc00000); idx = 0x7fffffff; }
-        else if (a.logits) a.logits[(size_t)b * a.logits_stride + n] = v;
-        warp_argmax(v, idx);
-        if (lane == 0) { bv[b] = v; bi[b] = idx; }
+        if constexpr (EPI == EPI_ARGMAX) {
+          const int n = rg * 32 + lane;
+          if (n < a.n_valid) {
+            const float v = fin[b * 32 + lane];
+            if (a.logits) a.logits[(size_t)b * a.logits_stride + n] = v;
+            if (argmax_better(v, n, best_v[b], best_i[b])) { best_v[b] = v; best_i[b] = n; }
+          }
+        } else if constexpr (EPI == EPI_GEGLU) {
+          const int n = rg * 32 + lane;  // R == 2: block 0 = gate rows, block 1 = up rows
+          if (n < a.n_valid) {
+            const float g = fin[(0 * NB + b) * 32 + lane], u = fin[(1 * NB + b) * 32 + lane];
+            a.y[(size_t)b * a.y_stride + n] = gelu_tanh(g) * u;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int n = (rg * R + r) * 32 + lane;
+            if (n >= a.n_valid) continue;
+            float v = fin[(r * NB + b) * 32 + lane];
+            if constexpr (EPI == EPI_PLE) v = gelu_tanh(v) * a.ple[(size_t)b * a.ple_stride + n];
+            a.y[(size_t)b * a.y_stride + n] = v;
+          }
+        }
       }
     }
-    __syncthreads();
-    if (threadIdx.x < a.nb) {
-      a.am_val[threadIdx.x * gridDim.x + blockIdx.x] = bv[threadIdx.x];
-      a.am_idx[threadIdx.x * gridDim.x + blockIdx.x] = bi[threadIdx.x];
+    __syncthreads();  // red/fin reuse by the next row group
+  }
+
+  if constexpr (EPI == EPI_ARGMAX) {
+    // CTA partial (warp 0 holds the running bests), then the last CTA reduces all partials.
+    __shared__ int is_last_am;
+    if (warp == 0) {
+      for (int b = 0; b < a.nb; ++b) {
+        float v = best_v[b];
+        int i = best_i[b];
+        warp_argmax(v, i);
+        if (lane == 0) {
+          a.am_val[b * gridDim.x + blockIdx.x] = v;
+          a.am_idx[b * gridDim.x + blockIdx.x] = i;
+        }
+      }
     }
     __threadfence();
     __syncthreads();
-    __shared__ int is_last_am;
-    unsigned* cnt = a.counters + gridDim.x;  // one past the per-row-group counters
-    if (threadIdx.x == 0) is_last_am = (atomicAdd(cnt, 1u) == gridDim.x - 1);
+    unsigned* cnt = a.counters + n_rg;  // one past the per-row-group counters
+    if (threadIdx.x == 0) is_last_am = atomicAdd(cnt, 1u) == gridDim.x - 1;
     __syncthreads();
     if (!is_last_am) return;
     __threadfence();
@@ -342,8 +409,8 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
       float v = __int_as_float(0x7fc00000);
       int idx = 0x7fffffff;
       for (int c = threadIdx.x; c < (int)gridDim.x; c += blockDim.x) {
-        float cv = ldcg(a.am_val + b * gridDim.x + c);
-        int ci = __ldcg(a.am_idx + b * gridDim.x + c);
+        const float cv = ldcg(a.am_val + b * gridDim.x + c);
+        const int ci = __ldcg(a.am_idx + b * gridDim.x + c);
         if (argmax_better(cv, ci, v, idx)) { v = cv; idx = ci; }
       }
       warp_argmax(v, idx);
@@ -357,37 +424,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
       __syncthreads();
     }
     if (threadIdx.x == 0) *cnt = 0u;
-  } else {
-    if (warp != 0) return;
-    for (int b = 0; b < a.nb; ++b) {
-      if constexpr (EPI == EPI_GEGLU) {
-        const int n = rg * 32 + lane;  // R == 2: block 0 = gate rows, block 1 = up rows
-        if (n < a.n_valid) {
-          const float g = fin[(0 * NB + b) * 32 + lane], u = fin[(1 * NB + b) * 32 + lane];
-          a.y[(size_t)b * a.y_stride + n] = gelu_tanh(g) * u;
-        }
-      } else {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const int n = (rg * R + r) * 32 + lane;
-          if (n >= a.n_valid) continue;
-          float v = fin[(r * NB + b) * 32 + lane];
-          if constexpr (EPI == EPI_PLE) v = gelu_tanh(v) * a.ple[(size_t)b * a.ple_stride + n];
-          a.y[(size_t)b * a.y_stride + n] = v;
-        }
-      }
-    }
   }
-}
-
-// Shared memory bytes of one launch.
-template <int FMT, int R, int NB>
-inline size_t gemv_smem_bytes(int sg_per_cta) {
-  const int kc = sg_per_cta * Fmt<FMT>::SGK;
-  const int nv = R * NB * 32;
-  size_t red = (size_t)(kGemvWarps + 1) * nv;
-  if (red < 32 * NB) red = 32 * NB;
-  return ((size_t)NB * kc + red) * sizeof(float);
 }
 
 }  // namespace g4

@@ -19,17 +19,36 @@ struct EmbedArgs {
   int* err;
 };
 
+// Grid (ceil((H + LP) / (8 * blockDim.x)), nb): each thread converts 8 bf16 (one 16-byte load).
 __global__ void embed_kernel(const EmbedArgs a) {
-  const int b = blockIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.y;
   int t = a.idx ? a.tokens[a.idx[b]] : a.tokens[b];
   if (t < 0 || t >= a.V) {
-    if (threadIdx.x == 0) set_err(a.err, G4_DEV_BAD_TOKEN);
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_err(a.err, G4_DEV_BAD_TOKEN);
     t = 0;
   }
-  const __nv_bfloat16* e = a.embed + (size_t)t * a.H;
-  for (int k = threadIdx.x; k < a.H; k += blockDim.x) a.x0[(size_t)b * a.H + k] = bf16f(e[k]) * a.sqrt_h;
-  const __nv_bfloat16* p = a.ple_table + (size_t)t * a.LP;
-  for (int k = threadIdx.x; k < a.LP; k += blockDim.x) a.tok[(size_t)b * a.LP + k] = bf16f(p[k]) * a.sqrt_p;
+  const int i8 = (blockIdx.x * blockDim.x + threadIdx.x) * 8;  // element index over [x0 | tok]
+  const __nv_bfloat16* src;
+  float* dst;
+  float sc;
+  if (i8 < a.H) {
+    src = a.embed + (size_t)t * a.H + i8;
+    dst = a.x0 + (size_t)b * a.H + i8;
+    sc = a.sqrt_h;
+  } else if (i8 < a.H + a.LP) {
+    src = a.ple_table + (size_t)t * a.LP + (i8 - a.H);
+    dst = a.tok + (size_t)b * a.LP + (i8 - a.H);
+    sc = a.sqrt_p;
+  } else {
+    return;
+  }
+  const uint4 u = *reinterpret_cast<const uint4*>(src);
+  const float4 lo = make_float4(bf16_lo(u.x) * sc, bf16_hi(u.x) * sc, bf16_lo(u.y) * sc, bf16_hi(u.y) * sc);
+  const float4 hi = make_float4(bf16_lo(u.z) * sc, bf16_hi(u.z) * sc, bf16_lo(u.w) * sc, bf16_hi(u.w) * sc);
+  reinterpret_cast<float4*>(dst)[0] = lo;
+  reinterpret_cast<float4*>(dst)[1] = hi;
 }
 
 // ple[b][l] = (RMSNorm(pr[b][l] * H^-1/2) * g + tok[b][l]) * 2^-1/2, one block per (b, l).
@@ -37,6 +56,8 @@ __global__ void embed_kernel(const EmbedArgs a) {
 __global__ void ple_combine_kernel(const float* pr, const float* tok, const __nv_bfloat16* g, int L, int P,
                                    float inv_sqrt_h, float inv_sqrt2, float eps, float* ple) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.y, l = blockIdx.x;
   const size_t base = ((size_t)b * L + l) * P;
   float ss[1] = {0.f};

@@ -32,11 +32,18 @@ CONFIGS = {
     "tiny10": dict(_OPEN, name="tiny10", num_layers=10, num_kv_shared_layers=4, hidden=256,
                    num_q_heads=4, head_dim_sliding=64, head_dim_full=128, sliding_window=64,
                    mlp=512, mlp_shared=1024, ple_dim=32, vocab=4096),
+    # E2B head dims, window and MQA layout at a small width: long contexts in seconds.
+    "mid": dict(_OPEN, name="mid", num_layers=10, num_kv_shared_layers=4, hidden=512,
+                num_q_heads=8, head_dim_sliding=256, head_dim_full=512, sliding_window=512,
+                mlp=1024, mlp_shared=2048, ple_dim=64, vocab=8192),
     # E2B-shaped.
     "e2b": dict(_OPEN, name="e2b", num_layers=35, num_kv_shared_layers=20, hidden=1536,
                 num_q_heads=8, head_dim_sliding=256, head_dim_full=512, sliding_window=512,
                 mlp=6144, mlp_shared=12288, ple_dim=256, vocab=262144),
 }
+# E2B layer shapes with an 8,192-entry vocabulary: every per-layer kernel is E2B's, while the
+# whole model holds about 1 GB (small enough for multi-pass profiler captures).
+CONFIGS["e2b-v8k"] = dict(CONFIGS["e2b"], name="e2b-v8k", vocab=8192)
 
 
 def get_config(name):
@@ -67,6 +74,7 @@ for _fmt in ("bf16", "w4a16"):
     for _b in (8, 16, 32, 64):
         WORKLOADS[f"e2b-{_fmt}-b{_b}"] = dict(config="e2b", fmt=_fmt, batch=_b, prompt=128,
                                                out=512)
+WORKLOADS["e2b-v8k-w4a16-b1"] = dict(config="e2b-v8k", fmt="w4a16", batch=1, prompt=128, out=512)
 # Agent replay: batch 8, 500-token start, 20 turns of 375 appended tokens + 32 outputs.
 WORKLOADS["e2b-w4a16-replay-b8"] = dict(config="e2b", fmt="w4a16", batch=8, prompt=500,
                                         out=32, turns=20, turn_append=375)
