@@ -28,6 +28,7 @@
 
 #include "attn.cuh"
 #include "common.cuh"
+#include "gemm_tc.cuh"
 #include "gemv.cuh"
 #include "misc.cuh"
 
@@ -108,6 +109,10 @@ struct g4_handle {
   float* am_val = nullptr;
   int* am_idx = nullptr;
   size_t am_n = 0;
+  uint8_t* xt = nullptr;  // tensor-core GEMM activation tiles
+  size_t xt_bytes = 0;
+  float* tc_part = nullptr;
+  size_t tc_part_floats = 0;
   float *attn_ml = nullptr, *attn_o = nullptr;
   unsigned* attn_cnt = nullptr;
   size_t attn_ml_n = 0, attn_o_n = 0;
@@ -192,7 +197,7 @@ g4_status build_lin(g4_handle* h, int fmt, int K, const std::vector<Seg>& segs, 
     for (const Seg& s : segs) { seg_blocks(s, rbs); n += s.rows; }
     L.n_valid = n;
   }
-  while (rbs.size() % L.R) rbs.push_back(RbSrc{nullptr, nullptr, 0, 0});
+  while (rbs.size() % 4) rbs.push_back(RbSrc{nullptr, nullptr, 0, 0});  // M tiles of 128 rows
   L.n_rb = (int)rbs.size();
   L.N = L.n_rb * 32;
   L.S = cdiv(K, sgk(fmt));
@@ -312,6 +317,8 @@ int init_kernel_attrs(int device) {
   attrs_gemv<FMT_W4A16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_ARGMAX>(optin);
+  set_max_dyn(gemm_tc_kernel, optin);
+  set_max_dyn(prep_x_kernel, optin);
   attrs_attn<64>(optin);
   attrs_attn<128>(optin);
   attrs_attn<256>(optin);
@@ -344,9 +351,90 @@ int gemv_grid(const Lin& L, int sms) {
   return std::min(n_rg, 4 * sms);
 }
 
+// Tensor-core path for batches >= G4_TC_MIN_BATCH (default 16; 0 disables it).
+int tc_min_batch() {
+  static const int v = [] {
+    const char* e = getenv("G4_TC_MIN_BATCH");
+    return e ? atoi(e) : 16;
+  }();
+  return v;
+}
+int tc_bpad(int n) { return (n + 15) / 16 * 16; }
+int tc_nkb(const Lin& L) { return cdiv(L.K, kTcKB); }
+// K split so that M tiles x splits roughly fill the SMs once (one CTA per SM).
+void tc_plan(const Lin& L, int sms, bool whole_k, int* ksplit, int* kbps) {
+  const int nmt = L.n_rb / 4, nkb = tc_nkb(L);
+  int k = whole_k ? 1 : std::max(1, std::min(nkb, sms / std::max(1, nmt)));
+  *kbps = cdiv(nkb, k);
+  *ksplit = cdiv(nkb, *kbps);
+}
+
+struct TcScratch {
+  uint8_t* xt;
+  float* part;
+  unsigned* cnt;
+  float* am_val;
+  int* am_idx;
+  int* err;
+};
+
+void run_gemm(const Lin& L, int epi, const GemvIO& io, int n, float eps, const TcScratch& s, int sms, cudaStream_t st) {
+  const int bpad = tc_bpad(n), nkb = tc_nkb(L);
+  PrepArgs p{};
+  p.pro = io.pro;
+  p.x_in = io.x_in;
+  p.x_stride = io.x_stride;
+  p.r_in = io.r_in;
+  p.r_stride = io.r_stride;
+  p.g_r = io.g_r;
+  p.lambda = io.lambda;
+  p.g_a = io.g_a;
+  p.x_out = io.x_out;
+  p.eps = eps;
+  p.K = L.K;
+  p.kpad = nkb * kTcKB;
+  p.bpad = bpad;
+  p.xt = s.xt;
+  launch(prep_x_kernel, dim3(n), dim3(256), (size_t)p.kpad * 4, st, p);
+  GemmArgs g{};
+  g.qw = L.qw;
+  g.sc = L.sc;
+  g.fmt = L.fmt == G4_W4A16 ? FMT_W4A16 : FMT_BF16;
+  g.tiles = L.tiles;
+  g.S = L.S;
+  g.n_valid = L.n_valid;
+  g.n_kb = nkb;
+  tc_plan(L, sms, epi == EPI_ARGMAX, &g.ksplit, &g.kb_per_split);
+  g.xt = s.xt;
+  g.bpad = bpad;
+  g.nb = n;
+  g.epi = epi;
+  g.y = io.y;
+  g.y_stride = io.y_stride;
+  g.ple = io.ple;
+  g.ple_stride = io.ple_stride;
+  g.logits = io.logits;
+  g.logits_stride = io.logits_stride;
+  g.am_val = s.am_val;
+  g.am_idx = s.am_idx;
+  g.part = s.part;
+  g.counters = s.cnt;
+  g.n_mtiles = L.n_rb / 4;
+  g.err = s.err;
+  const int grid = g.n_mtiles * g.ksplit;
+  launch(gemm_tc_kernel, dim3(grid), dim3(kTcThreads), tc_smem_bytes(bpad), st, g);
+  if (epi == EPI_ARGMAX)
+    launch(argmax_partials_kernel, dim3(n), dim3(256), 0, st, (const float*)s.am_val, (const int*)s.am_idx, grid,
+           io.next_ids);
+}
+
 // y = W x for n rows, in chunks of kMaxNB rows.
 void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const Scratch& s, int sms,
-              cudaStream_t st) {
+              cudaStream_t st, const TcScratch* tc = nullptr) {
+  if (tc && tc_min_batch() > 0 && n >= tc_min_batch() && n <= 64) {
+    run_gemm(L, epi, io, n, eps, *tc, sms, st);
+    return;
+  }
   for (int b0 = 0; b0 < n; b0 += kMaxNB) {
     const int nb = std::min(kMaxNB, n - b0);
     GemvArgs a{};
@@ -468,6 +556,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
   const float eps = c.rms_eps;
   Scratch s{h->gemv_part, h->gemv_cnt, h->am_val, h->am_idx};
+  TcScratch tc{h->xt, h->tc_part, h->gemv_cnt, h->am_val, h->am_idx, h->err};
 
   EmbedArgs ea{d_tokens, d_idx, h->embed, h->ple_table, c.vocab, H, LP,
                (float)std::sqrt((double)H), (float)std::sqrt((double)P), h->x0, h->tok, h->err};
@@ -483,7 +572,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
     io.x_stride = H;
     io.y = h->pr;
     io.y_stride = LP;
-    run_gemv(h->pmp, EPI_STORE, io, n, eps, s, h->sms, st);
+    run_gemv(h->pmp, EPI_STORE, io, n, eps, s, h->sms, st, &tc);
   }
   {
     ProfScope ps(prof, "ple_combine", 0.0);
@@ -519,7 +608,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y_stride = Y.qkv.n_valid;
       {
         ProfScope ps(prof, "gemv.qkv", (double)Y.qkv.bytes);
-        run_gemv(Y.qkv, EPI_STORE, io, n, eps, s, h->sms, st);
+        run_gemv(Y.qkv, EPI_STORE, io, n, eps, s, h->sms, st, &tc);
       }
       if (l > 0) {
         cur = io.x_out;
@@ -579,7 +668,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y = h->r_attn;
       io.y_stride = H;
       ProfScope ps(prof, "gemv.o", (double)Y.o.bytes);
-      run_gemv(Y.o, EPI_STORE, io, n, eps, s, h->sms, st);
+      run_gemv(Y.o, EPI_STORE, io, n, eps, s, h->sms, st, &tc);
     }
     {  // gate/up
       GemvIO io;
@@ -597,7 +686,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y_stride = Y.F;
       {
         ProfScope ps(prof, "gemv.gate_up", (double)Y.gu.bytes);
-        run_gemv(Y.gu, EPI_GEGLU, io, n, eps, s, h->sms, st);
+        run_gemv(Y.gu, EPI_GEGLU, io, n, eps, s, h->sms, st, &tc);
       }
       cur = io.x_out;
     }
@@ -609,7 +698,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y = h->r_mlp;
       io.y_stride = H;
       ProfScope ps(prof, "gemv.down", (double)Y.down.bytes);
-      run_gemv(Y.down, EPI_STORE, io, n, eps, s, h->sms, st);
+      run_gemv(Y.down, EPI_STORE, io, n, eps, s, h->sms, st, &tc);
     }
     {  // PLE gate
       GemvIO io;
@@ -629,7 +718,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.ple_stride = LP;
       {
         ProfScope ps(prof, "gemv.ple_gate", (double)Y.pg.bytes);
-        run_gemv(Y.pg, EPI_PLE, io, n, eps, s, h->sms, st);
+        run_gemv(Y.pg, EPI_PLE, io, n, eps, s, h->sms, st, &tc);
       }
       cur = io.x_out;
     }
@@ -641,7 +730,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.y = h->r_ple;
       io.y_stride = H;
       ProfScope ps(prof, "gemv.ple_proj", (double)Y.pp.bytes);
-      run_gemv(Y.pp, EPI_STORE, io, n, eps, s, h->sms, st);
+      run_gemv(Y.pp, EPI_STORE, io, n, eps, s, h->sms, st, &tc);
     }
   }
   {  // final norm, lm_head, argmax
@@ -662,7 +751,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
     io.next_ids = d_next;
     {
       ProfScope ps(prof, "gemv.lm_head_argmax", (double)h->lm.bytes);
-      run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, h->sms, st);
+      run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, h->sms, st, &tc);
     }
     if (h->trace)
       for (int i = 0; i < n; ++i)
@@ -816,12 +905,30 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
     for (const Lin* Ln : {&Y.qkv, &Y.o, &Y.gu, &Y.down, &Y.pg, &Y.pp}) acc_lin(*Ln);
   acc_lin(h->pmp);
   acc_lin(h->lm);
+  // tensor-core GEMM scratch: activation tiles for the widest K, split-K partials
+  size_t xtb = 16, tcp = 1;
+  auto acc_tc = [&](const Lin& Ln, bool whole) {
+    int ks, kbps;
+    tc_plan(Ln, h->sms, whole, &ks, &kbps);
+    xtb = std::max(xtb, (size_t)tc_nkb(Ln) * 2 * 64 * 128);
+    tcp = std::max(tcp, (size_t)ks * 64 * (Ln.n_rb / 4) * 128);
+    cnt = std::max(cnt, (size_t)(Ln.n_rb / 4) + 1);
+  };
+  for (const Layer& Y : h->layers)
+    for (const Lin* Ln : {&Y.qkv, &Y.o, &Y.gu, &Y.down, &Y.pg, &Y.pp}) acc_tc(*Ln, false);
+  acc_tc(h->pmp, false);
+  acc_tc(h->lm, true);
+  h->xt_bytes = xtb;
+  h->tc_part_floats = tcp;
+  TRY(dalloc(h, &h->xt, xtb));
+  CK(cudaMemsetAsync(h->xt, 0, xtb, st));
+  TRY(dalloc(h, &h->tc_part, tcp));
   h->gemv_part_floats = part;
   h->gemv_cnt_n = cnt;
   TRY(dalloc(h, &h->gemv_part, part));
   TRY(dalloc(h, &h->gemv_cnt, cnt));
   CK(cudaMemsetAsync(h->gemv_cnt, 0, cnt * sizeof(unsigned), st));
-  h->am_n = (size_t)kMaxNB * (h->lm.n_rb / h->lm.R) * h->lm.ksplit;
+  h->am_n = std::max((size_t)kMaxNB * (h->lm.n_rb / h->lm.R) * h->lm.ksplit, (size_t)64 * (h->lm.n_rb / 4));
   TRY(dalloc(h, &h->am_val, h->am_n));
   TRY(dalloc(h, &h->am_idx, h->am_n));
   // attention scratch for the largest (nb * nsplit) over batch sizes
@@ -1094,9 +1201,16 @@ g4_status g4_linear_create(int device, int32_t weight_format, int32_t n_out, int
     plan_lin(op->lin, op->h.sms, false);
     size_t part = (size_t)op->lin.ksplit * kMaxNB * op->lin.n_rb * 32;
     size_t cnt = (size_t)op->lin.n_rb * op->lin.ksplit + 1;
+    int ks, kbps;
+    tc_plan(op->lin, op->h.sms, false, &ks, &kbps);
+    cnt = std::max(cnt, (size_t)(op->lin.n_rb / 4) + 1);
     s = dalloc(&op->h, &op->h.gemv_part, part);
     if (s == G4_OK) s = dalloc(&op->h, &op->h.gemv_cnt, cnt);
     if (s == G4_OK && !cuda_ok(cudaMemsetAsync(op->h.gemv_cnt, 0, cnt * 4, st), "memset")) s = G4_ERR_CUDA;
+    if (s == G4_OK) s = dalloc(&op->h, &op->h.xt, (size_t)tc_nkb(op->lin) * 2 * 64 * 128);
+    if (s == G4_OK) s = dalloc(&op->h, &op->h.tc_part, (size_t)ks * 64 * (op->lin.n_rb / 4) * 128);
+    if (s == G4_OK) s = dalloc(&op->h, &op->h.err, 1);
+    if (s == G4_OK && !cuda_ok(cudaMemsetAsync(op->h.err, 0, 4, st), "memset")) s = G4_ERR_CUDA;
   }
   cudaStreamSynchronize(st);
   cudaStreamDestroy(st);
@@ -1119,7 +1233,8 @@ g4_status g4_linear_forward(g4_linear_op* op, g4_stream stream, int32_t n_rows, 
   io.y = d_y;
   io.y_stride = op->lin.n_valid;
   Scratch s{op->h.gemv_part, op->h.gemv_cnt, nullptr, nullptr};
-  run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, op->h.sms, reinterpret_cast<cudaStream_t>(stream));
+  TcScratch tc{op->h.xt, op->h.tc_part, op->h.gemv_cnt, nullptr, nullptr, op->h.err};
+  run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, op->h.sms, reinterpret_cast<cudaStream_t>(stream), &tc);
   CK(cudaGetLastError());
   return G4_OK;
 }

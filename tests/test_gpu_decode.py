@@ -235,3 +235,20 @@ def test_errors_host_and_device(rt):
     torch.cuda.synchronize()
     assert dec.device_error() == (g4.G4_OK, 0)
     dec.close()
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "w4a16"])
+def test_batch16_tensor_core_path(rt, fmt):
+    """Batch 16 and 19: every projection and the lm_head run on the tcgen05 GEMM."""
+    cfg = synth.get_config("tiny10")
+    w = synth.make_weights(cfg, fmt, seed=12, gain_std=0.1)
+    for nb in (16, 19):
+        prompts = synth.make_prompts(cfg["vocab"], nb, 6, seed=nb)
+        ref = oracle.Oracle(cfg, w, max_batch=nb, max_context=32).generate(prompts, 4, keep_logits=True)
+        dec = rt.Decoder(cfg, w, max_batch=nb, max_context=32)
+        toks, logits = gpu_generate(dec, list(prompts), 4, teacher=ref["tokens"])
+        assert dec.device_error()[1] == 0
+        dec.close()
+        assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL
+        ok = ref["gaps"].T > GAP_TIE
+        assert np.all((toks == ref["tokens"]) | ~ok)

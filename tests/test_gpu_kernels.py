@@ -122,3 +122,25 @@ def test_argmax_rows_ignores_nan(rt):
     x[0, 4100] = 2.0
     x[0, 17] = 2.0
     assert rt.argmax_rows(torch.from_numpy(x).cuda()).cpu().numpy().tolist() == [17]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "w4a16"])
+@pytest.mark.parametrize("shape", [(128, 64), (96, 288), (2560, 1536), (1536, 2048), (1536, 6144),
+                                   (8960, 1536), (12288, 1536), (1536, 256), (256, 1536)])
+def test_linear_tensor_core_batches(rt, fmt, shape):
+    """Batches >= 16 run the tcgen05 dequant GEMM (bf16 x_hi + x_lo against bf16(q*s), fp32
+    accumulation in TMEM); it must match the oracle's dense product like the GEMV does."""
+    n_out, n_in = shape
+    lin = _linear(fmt, n_out, n_in, seed=n_out * 3 + n_in)
+    W = _dense(fmt, lin)
+    op = rt.LinearOp(fmt, lin)
+    rng = np.random.default_rng(n_out - n_in)
+    for nb in (16, 17, 40, 64):
+        x = rng.standard_normal((nb, n_in)).astype(np.float32)
+        y = op(torch.from_numpy(x).cuda()).cpu().numpy()
+        ref = x.astype(np.float64) @ W.T
+        # x_lo leaves |x| * 2^-17 per element; fp32 accumulation adds the rest
+        bound = 4e-5 * (np.abs(x).astype(np.float64) @ np.abs(W).T) + 1e-6
+        assert np.all(np.abs(y - ref) <= bound), (fmt, shape, nb, np.max(np.abs(y - ref) / bound))
+        np.testing.assert_allclose(y, ref, rtol=1e-2, atol=1e-4 * np.max(np.abs(ref)))
+    op.close()
