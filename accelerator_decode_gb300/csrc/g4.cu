@@ -364,7 +364,8 @@ int tc_nkb(const Lin& L) { return cdiv(L.K, kTcKB); }
 // K split so that M tiles x splits roughly fill the SMs once (one CTA per SM).
 void tc_plan(const Lin& L, int sms, bool whole_k, int* ksplit, int* kbps) {
   const int nmt = L.n_rb / 4, nkb = tc_nkb(L);
-  int k = whole_k ? 1 : std::max(1, std::min(nkb, sms / std::max(1, nmt)));
+  // at least 4 k-blocks per split: the split-K reduction is not free
+  int k = whole_k ? 1 : std::max(1, std::min(cdiv(nkb, 4), sms / std::max(1, nmt)));
   *kbps = cdiv(nkb, k);
   *ksplit = cdiv(nkb, *kbps);
 }
@@ -395,7 +396,7 @@ void run_gemm(const Lin& L, int epi, const GemvIO& io, int n, float eps, const T
   p.kpad = nkb * kTcKB;
   p.bpad = bpad;
   p.xt = s.xt;
-  launch(prep_x_kernel, dim3(n), dim3(256), (size_t)p.kpad * 4, st, p);
+  launch(prep_x_kernel, dim3(n), dim3(256), (size_t)p.kpad * 2 * 4, st, p);
   GemmArgs g{};
   g.qw = L.qw;
   g.sc = L.sc;

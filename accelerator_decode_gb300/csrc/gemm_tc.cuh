@@ -314,8 +314,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     const int rows_total = a.n_mtiles * kTcM;
     bool final_ok = have;
     if (a.ksplit > 1) {
-      if (have)
-        for (int b = 0; b < a.nb; ++b) a.part[((size_t)ks * a.nb + b) * rows_total + row] = v[b];
+      if (have) {
+#pragma unroll
+        for (int b = 0; b < 64; ++b)
+          if (b < a.nb) a.part[((size_t)ks * a.nb + b) * rows_total + row] = v[b];
+      }
       __threadfence();
       asm volatile("bar.sync 1, 128;\n" ::: "memory");
       if (m == 0) *is_last_s = atomicAdd(&a.counters[mt], 1u) == (unsigned)a.ksplit - 1;
@@ -323,10 +326,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
       final_ok = *is_last_s != 0;
       if (final_ok) {
         __threadfence();
-        for (int b = 0; b < a.nb; ++b) {
-          float sum = 0.f;
-          for (int q = 0; q < a.ksplit; ++q) sum += ldcg(a.part + ((size_t)q * a.nb + b) * rows_total + row);
-          v[b] = sum;
+#pragma unroll
+        for (int b = 0; b < 64; ++b) v[b] = 0.f;
+        for (int q = 0; q < a.ksplit; ++q) {  // split order: deterministic; 64 loads in flight
+          const float* pq = a.part + (size_t)q * a.nb * rows_total + row;
+#pragma unroll
+          for (int b = 0; b < 64; ++b)
+            if (b < a.nb) v[b] += ldcg(pq + (size_t)b * rows_total);
         }
         if (m == 0) a.counters[mt] = 0u;
       }
@@ -337,7 +343,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
         const int pair = warp >> 1;
         const bool is_up = warp & 1;
         const int n = mt * 64 + pair * 32 + ln;
-        for (int b = 0; b < a.nb; ++b) {
+#pragma unroll
+        for (int b = 0; b < 64; ++b) {
+          if (b >= a.nb) break;
           if (is_up) xch[pair * 32 + ln] = v[b];
           asm volatile("bar.sync 1, 128;\n" ::: "memory");
           if (!is_up && n < a.n_valid) a.y[(size_t)b * a.y_stride + n] = gelu_tanh(v[b]) * xch[pair * 32 + ln];
@@ -347,7 +355,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
         // per column b: max over this tile's rows -> one partial per (b, CTA)
         float* bv = xch;                                   // [4] per warp
         int* bi = reinterpret_cast<int*>(xch + 4);
-        for (int b = 0; b < a.nb; ++b) {
+#pragma unroll
+        for (int b = 0; b < 64; ++b) {
+          if (b >= a.nb) break;
           float x = v[b];
           int idx = row;
           if (row >= a.n_valid) { x = __int_as_float(0x7fc00000); idx = 0x7fffffff; }
@@ -364,7 +374,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
           asm volatile("bar.sync 1, 128;\n" ::: "memory");
         }
       } else if (row < a.n_valid) {
-        for (int b = 0; b < a.nb; ++b) {
+#pragma unroll
+        for (int b = 0; b < 64; ++b) {
+          if (b >= a.nb) break;
           float o = v[b];
           if (a.epi == EPI_PLE) o = gelu_tanh(o) * a.ple[(size_t)b * a.ple_stride + row];
           a.y[(size_t)b * a.y_stride + row] = o;
@@ -408,10 +420,16 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const PrepArgs a) {
   pdl_wait();
   const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   const float* x = a.x_in + (size_t)b * a.x_stride;
-  for (int k = tid; k < a.kpad; k += nt) prow[k] = k < a.K ? x[k] : 0.f;
+  float* rrow = prow + a.kpad;  // [K] residual branch (PRO_RESID)
+  for (int c = tid; c < a.kpad / 4; c += nt) {
+    const bool ok = 4 * c < a.K;
+    cp_async16(prow + 4 * c, ok ? x + 4 * c : x, ok);
+    if (a.pro == PRO_RESID && ok) cp_async16(rrow + 4 * c, a.r_in + (size_t)b * a.r_stride + 4 * c, true);
+  }
+  cp_async_wait_all();
   __syncthreads();
   if (a.pro == PRO_RESID) {
-    const float* r = a.r_in + (size_t)b * a.r_stride;
+    const float* r = rrow;
     float ss[1] = {0.f};
     for (int k = tid; k < a.K; k += nt) ss[0] += r[k] * r[k];
     block_sum<1>(ss, red);

@@ -75,6 +75,7 @@ for _fmt in ("bf16", "w4a16"):
         WORKLOADS[f"e2b-{_fmt}-b{_b}"] = dict(config="e2b", fmt=_fmt, batch=_b, prompt=128,
                                                out=512)
 WORKLOADS["e2b-v8k-w4a16-b1"] = dict(config="e2b-v8k", fmt="w4a16", batch=1, prompt=128, out=512)
+WORKLOADS["e2b-v8k-w4a16-b64"] = dict(config="e2b-v8k", fmt="w4a16", batch=64, prompt=128, out=512)
 # Agent replay: batch 8, 500-token start, 20 turns of 375 appended tokens + 32 outputs.
 WORKLOADS["e2b-w4a16-replay-b8"] = dict(config="e2b", fmt="w4a16", batch=8, prompt=500,
                                         out=32, turns=20, turn_append=375)
