@@ -52,6 +52,12 @@ def max_over_ranks(value, world, device=None):
     return float(t.item())
 
 
+def replica_throughput(world, batch, steps, ms_max):
+    """Whole-job tok/s of `world` replicas that each decode `batch` sequences for `steps`
+    steps, timed by the slowest rank (ms_max)."""
+    return world * batch * steps / (ms_max / 1e3)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -307,7 +313,7 @@ def run_gpu(args, wl, cfg, fmt):
     wbytes, kvbytes = algorithmic_bytes(cfg, fmt, B, positions)
     peak, peak_src = measured_peak()
     step_bytes = wbytes + kvbytes
-    value = world * B * K / (ms_max / 1e3)
+    value = replica_throughput(world, B, K, ms_max)
     reps = args.profile_repeats
     launches_per_step = sum(p["launches"] for p in prof) / reps
     prof_ms = sum(p["ms_total"] for p in prof) / reps
@@ -342,7 +348,8 @@ def run_gpu(args, wl, cfg, fmt):
                           "achieved": round(step_bytes / (ms_max / K / 1e3) / 1e9, 1), "peak": peak,
                           "frac": round(step_bytes / (ms_max / K / 1e3) / 1e9 / peak, 4), "unit": "GB/s",
                           "peak_source": peak_src, "calibrated_copy_gbs": round(copy_gbs, 1)},
-        "e2e": {"value": round(world * B * K / e2e_s, 2), "unit": "tok/s", "h2d_bytes_per_step": 2 * 4 * B,
+        "e2e": {"value": round(replica_throughput(world, B, K, e2e_s * 1e3), 2), "unit": "tok/s",
+                "h2d_bytes_per_step": 2 * 4 * B,
                 "d2h_bytes_per_step": 4 * B},
         "gpu_launches": int(round(launches_per_step * K)),
         "kernels_per_step": launches_per_step,
