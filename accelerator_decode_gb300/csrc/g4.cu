@@ -1290,4 +1290,54 @@ g4_status g4_argmax_rows(int device, g4_stream stream, int32_t n_rows, int32_t n
   return G4_OK;
 }
 
+// ---------------------------------------------------------------- argmax without allocation
+// Scratch of the allocation-free argmax: per-block partial values and indices for up to
+// kStaticArgmaxRows rows x kStaticArgmaxChunks column chunks, and one counter per row.
+// Every GPU that loads the library holds this array until the process exits.
+constexpr int kStaticArgmaxRows = 64;
+constexpr int kStaticArgmaxChunks = 256;
+constexpr int kStaticArgmaxChunk = 4096;
+struct StaticArgmaxScratch {
+  float pv[kStaticArgmaxRows * kStaticArgmaxChunks];
+  int pi[kStaticArgmaxRows * kStaticArgmaxChunks];
+  unsigned cnt[kStaticArgmaxRows];
+};
+static __device__ __align__(256) StaticArgmaxScratch g4_static_argmax_scratch;
+
+namespace {
+std::mutex g_static_mu;
+std::map<int, StaticArgmaxScratch*> g_static_ptr;  // device -> device address of the array
+}  // namespace
+
+g4_status g4_argmax_rows_static(int device, g4_stream stream, int32_t n_rows, int32_t n_cols,
+                                const float* d_logits, int32_t* d_ids) {
+  if (!d_logits || !d_ids || n_rows < 1 || n_cols < 1) return G4_ERR_INVALID_ARG;
+  const int nchunk = cdiv(n_cols, kStaticArgmaxChunk);
+  if (n_rows > kStaticArgmaxRows || nchunk > kStaticArgmaxChunks) {
+    g_last_cuda = "g4_argmax_rows_static: at most 64 rows and 1,048,576 columns";
+    return G4_ERR_INVALID_ARG;
+  }
+  CK(cudaSetDevice(device));
+  StaticArgmaxScratch* sc = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    auto it = g_static_ptr.find(device);
+    if (it == g_static_ptr.end()) {
+      // The array's host-side name is not a device address: look the address up once per
+      // device, with that device current.
+      void* p = nullptr;
+      CK(cudaGetSymbolAddress(&p, g4_static_argmax_scratch));
+      it = g_static_ptr.emplace(device, static_cast<StaticArgmaxScratch*>(p)).first;
+    }
+    sc = it->second;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // counters must start at zero (an earlier call may have been cut short)
+  CK(cudaMemsetAsync(sc->cnt, 0, sizeof(unsigned) * n_rows, st));
+  argmax_rows_kernel<<<dim3(nchunk, n_rows), 256, 0, st>>>(d_logits, n_cols, kStaticArgmaxChunk, sc->pv, sc->pi,
+                                                           sc->cnt, d_ids);
+  CK(cudaGetLastError());
+  return G4_OK;
+}
+
 }  // extern "C"

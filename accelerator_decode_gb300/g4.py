@@ -94,6 +94,7 @@ def _load():
         "g4_linear_forward": (c_int, [P, P, c_int32, P, P]),
         "g4_linear_free": (None, [P]),
         "g4_argmax_rows": (c_int, [c_int, P, c_int32, c_int32, P, P]),
+        "g4_argmax_rows_static": (c_int, [c_int, P, c_int32, c_int32, P, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)

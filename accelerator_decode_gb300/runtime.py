@@ -175,3 +175,11 @@ def argmax_rows(logits, stream=None):
     _g4.check(_g4.lib.g4_argmax_rows(logits.device.index, stream_handle(stream), logits.shape[0],
                                      logits.shape[1], _ptr(logits), _ptr(ids)), "g4_argmax_rows")
     return ids
+
+
+def argmax_rows_static(logits, stream=None):
+    """Allocation-free row argmax (fixed scratch inside the library; see include/g4.h)."""
+    ids = torch.empty(logits.shape[0], dtype=torch.int32, device=logits.device)
+    _g4.check(_g4.lib.g4_argmax_rows_static(logits.device.index, stream_handle(stream), logits.shape[0],
+                                            logits.shape[1], _ptr(logits), _ptr(ids)), "g4_argmax_rows_static")
+    return ids

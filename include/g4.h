@@ -209,6 +209,24 @@ void g4_linear_free(g4_linear_op* op);
 g4_status g4_argmax_rows(int device, g4_stream stream, int32_t n_rows, int32_t n_cols,
                          const float* d_logits, int32_t* d_ids);
 
+/* Row-wise greedy argmax like g4_argmax_rows, for callers that must not allocate device
+ * memory: it calls no cudaMalloc, cudaFree or allocating library routine.  Such callers
+ * include a serving loop that has handed all device memory to its own pool (an allocation
+ * here would fail, or would synchronise the whole device in the middle of a step) and code
+ * running between a stream capture's begin and end, where cudaMalloc may not be called.
+ * (The pages have no counterpart: this is an interface convenience, not part of the method.)
+ *
+ * Its scratch is one fixed array in the library (about 129 KB), held by every GPU that
+ * loads the library until the process exits.  Limits: n_rows <= 64 and n_cols <= 1,048,576;
+ * larger sizes return G4_ERR_INVALID_ARG (g4_last_cuda_error names the limits) with no
+ * device work.  The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every call clears the
+ * array's counters with a memset on `stream` and then reuses the array, which keeps the
+ * last call's partial results: calls that overlap on the GPU (other streams, other
+ * threads) race on it and must be serialised by the caller. */
+g4_status g4_argmax_rows_static(int device, g4_stream stream, int32_t n_rows, int32_t n_cols,
+                                const float* d_logits, int32_t* d_ids);
+
 #ifdef __cplusplus
 }
 #endif
