@@ -50,16 +50,24 @@ struct AttnArgs {
 template <int D, int HPC>
 __host__ __device__ inline size_t attn_smem_bytes(int nstage) {
   return (size_t)nstage * 2 * kAttnTile * D * 2                      // K, V tiles (bf16)
-         + ((size_t)HPC * D + 2 * D + HPC * kAttnTile + 4 * HPC) * 4;  // q, new k/v, scores, stats
+         + ((size_t)HPC * D + 2 * D + HPC * kAttnTile + 4 * HPC) * 4   // q, new k/v, scores, stats
+         + (64 + 4) * 4;                                             // merge weights, last flag
 }
 
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// One (split, head group, sequence) unit on kAttnThreads threads; `asmem` holds
+// attn_smem_bytes<D, HPC>(a.nstage) bytes.  Called by attn_kernel and by the persistent step.
 template <int D, int HPC>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+// Threads [tid_base, tid_base + 128) run the unit and synchronise on named barrier bar_id.
+__device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, int b, unsigned char* asmem,
+                                          int tid_base, int bar_id) {
   constexpr int PL = D / 32;                                    // q/k elements per lane (scores)
   constexpr int PT = D >= kAttnThreads ? D / kAttnThreads : 1;  // output elements per thread
   static_assert(PL >= 2 && PL % 2 == 0, "head dim must be a multiple of 64");
   constexpr int TD = kAttnTile * D;
-  extern __shared__ __align__(16) unsigned char asmem[];
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(asmem);  // [nstage][TILE][D]
   __nv_bfloat16* Vs = Ks + (size_t)a.nstage * TD;                // [nstage][TILE][D]
   float* qs = reinterpret_cast<float*>(Vs + (size_t)a.nstage * TD);  // [HPC][D]
@@ -69,14 +77,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   float* resc = sc + HPC * kAttnTile;
   float* m_sh = resc + HPC;
   float* l_sh = m_sh + HPC;
+  float* wgt = l_sh + 2 * HPC;                           // [64]
+  int* is_last_p = reinterpret_cast<int*>(wgt + 64);
 
-  const int split = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x - tid_base, warp = tid >> 5, lane = tid & 31;
   const int h0 = hg * HPC;
   const int n_hg = a.nq / HPC;
 
-  pdl_trigger();
-  pdl_wait();
   int p = a.positions[b];
   const int slot = a.slots[b];
   bool bad = false;
@@ -189,7 +196,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     const int st = ti % a.nstage;
     if (a.nstage > 1 && ti + 1 < ntiles) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
     else asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    __syncthreads();
+    named_sync(bar_id, kAttnThreads);
     const __nv_bfloat16* Kt = Ks + (size_t)st * TD;
     const __nv_bfloat16* Vt = Vs + (size_t)st * TD;
     // scores: warp per key, lanes over D
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         if (lane == 0) sc[h * kAttnTile + jj] = (jj < tn) ? d * a.scale : -INFINITY;
       }
     }
-    __syncthreads();
+    named_sync(bar_id, kAttnThreads);
     // softmax statistics per head (warp per head)
 #pragma unroll
     for (int h = 0; h < HPC; ++h) {
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       m_run[h] = mn;
       l_run[h] = l_run[h] * r + ls;
     }
-    __syncthreads();
+    named_sync(bar_id, kAttnThreads);
     // P V: thread owns PT contiguous elements of each head's output
     if (tid * PT < D) {
 #pragma unroll
@@ -276,14 +283,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         }
       }
     }
-    __syncthreads();
+    named_sync(bar_id, kAttnThreads);
     if (a.nstage > 1 && ti + 2 < ntiles) load_tile(ti + 2);
     else if (a.nstage == 1 && ti + 1 < ntiles) load_tile(ti + 1);
   }
 #pragma unroll
   for (int h = 0; h < HPC; ++h)
     if ((h % (kAttnThreads / 32)) == warp && lane == 0) { m_sh[h] = m_run[h]; l_sh[h] = l_run[h]; }
-  __syncthreads();
+  named_sync(bar_id, kAttnThreads);
 
   float* outb = a.out + (size_t)b * a.out_stride;
   if (a.nsplit == 1) {
@@ -309,15 +316,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     }
   }
   __threadfence();
-  __syncthreads();
-  __shared__ int is_last;
-  if (tid == 0) is_last = atomicAdd(&a.counters[b * n_hg + hg], 1u) == (unsigned)a.nsplit - 1;
-  __syncthreads();
-  if (!is_last) return;
+  named_sync(bar_id, kAttnThreads);
+  if (tid == 0) *is_last_p = atomicAdd(&a.counters[b * n_hg + hg], 1u) == (unsigned)a.nsplit - 1;
+  named_sync(bar_id, kAttnThreads);
+  if (!*is_last_p) return;
   __threadfence();
   // merge: w_s = exp(m_s - M) per split (empty splits carry l = 0 and o = 0), then
   // o = sum_s w_s o_s / sum_s w_s l_s
-  __shared__ float wgt[64];
   for (int h = 0; h < HPC; ++h) {
     const size_t row0 = base_ml + (size_t)(h0 + h) * a.nsplit;
     if (warp == 0) {
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
       L = warp_sum(L);
       if (lane == 0) l_sh[h] = L;
     }
-    __syncthreads();
+    named_sync(bar_id, kAttnThreads);
     const float L = l_sh[h];
     if (tid * PT < D) {
       float o[PT];
@@ -359,9 +364,17 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 #pragma unroll
       for (int e = 0; e < PT; ++e) outb[(h0 + h) * D + tid * PT + e] = L > 0.f ? o[e] / L : 0.f;
     }
-    __syncthreads();
+    named_sync(bar_id, kAttnThreads);
   }
   if (tid == 0) a.counters[b * n_hg + hg] = 0u;
+}
+
+template <int D, int HPC>
+__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+  extern __shared__ __align__(16) unsigned char asmem_k[];
+  pdl_trigger();
+  pdl_wait();
+  attn_unit<D, HPC>(a, blockIdx.x, blockIdx.y, blockIdx.z, asmem_k, 0, 1);
 }
 
 }  // namespace g4

@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
+#include "mega.cuh"
 #include "misc.cuh"
 
 using namespace g4;
@@ -125,6 +126,14 @@ struct g4_handle {
   // trace
   float* trace = nullptr;
   int trace_stride = 0;
+  // persistent step (n <= 2)
+  bool mega_ok = false;
+  MegaPhase* mega_phases = nullptr;
+  int mega_n = 0, mega_grid = 0;
+  size_t mega_smem = 0;
+  unsigned* mega_bar = nullptr;
+  float *mega_am_val = nullptr;
+  int* mega_am_idx = nullptr;
   // graphs
   std::map<GraphKey, cudaGraphExec_t> graphs;
 };
@@ -318,6 +327,8 @@ int init_kernel_attrs(int device) {
   attrs_gemv<FMT_BF16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_ARGMAX>(optin);
   set_max_dyn(gemm_tc_kernel, optin);
+  set_max_dyn(mega_step_kernel<1>, optin);
+  set_max_dyn(mega_step_kernel<2>, optin);
   set_max_dyn(prep_x_kernel, optin);
   attrs_attn<64>(optin);
   attrs_attn<128>(optin);
@@ -551,8 +562,14 @@ struct ProfScope {
 };
 
 // ------------------------------------------------------------------------------- the step
+g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens,
+                        const int* d_idx, const int* d_pos, int* d_next, float* d_logits);
+bool mega_enabled();
+
 g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens, const int* d_idx,
                    const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr) {
+  if (h->mega_ok && mega_enabled() && n <= 2 && !h->trace && !prof)
+    return run_step_mega(h, st, n, d_slots, d_tokens, d_idx, d_pos, d_next, d_logits);
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
   const float eps = c.rms_eps;
@@ -763,6 +780,356 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
   return G4_OK;
 }
 
+// ------------------------------------------------------------------- persistent step
+bool mega_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("G4_MEGA");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+// Units of one projection phase: K slices of spu supergroups, wpu warps per unit, upc units
+// per CTA at a time.  Minimises rounds x supergroups per warp; ties go to fewer K slices.
+void mega_plan(const Lin& L, int G, bool allow_split, MegaPhase& ph) {
+  const int n_rg = L.n_rb / L.R;
+  long best_cost = -1;
+  for (int spu = 1; spu <= L.S; ++spu) {
+    if (L.S % spu) continue;
+    const int ks = L.S / spu;
+    if ((ks > 1 && !allow_split) || ks > 8) continue;
+    for (int wpu : {8, 4, 2, 1}) {
+      if (wpu > spu && wpu > 1) continue;
+      const int upc = kMegaWarps / wpu;
+      const long units = (long)n_rg * ks;
+      const long rounds = ((units + upc - 1) / upc + G - 1) / G;
+      const long cost = rounds * ((spu + wpu - 1) / wpu);
+      const bool better = best_cost < 0 || cost < best_cost || (cost == best_cost && ks < ph.ksplit);
+      if (better) {
+        best_cost = cost;
+        ph.spu = spu;
+        ph.wpu = wpu;
+        ph.upc = upc;
+        ph.ksplit = ks;
+        ph.n_units = (int)units;
+      }
+    }
+  }
+}
+
+void mega_lin(MegaPhase& ph, const Lin& L) {
+  ph.qw = L.qw;
+  ph.sc = L.sc;
+  ph.fmt = L.fmt == G4_W4A16 ? FMT_W4A16 : FMT_BF16;
+  ph.R = L.R;
+  ph.n_rb = L.n_rb;
+  ph.tiles = L.tiles;
+  ph.S = L.S;
+  ph.K = L.K;
+  ph.n_valid = L.n_valid;
+}
+
+g4_status build_mega(g4_handle* h, cudaStream_t st) {
+  const g4_config& c = h->cfg;
+  const int H = c.hidden, L = c.num_layers, P = c.ple_dim, nq = c.num_q_heads;
+  const int G = h->sms, NB = 2;
+  if (h->lm.S > 32 || H % 8) return G4_OK;  // lm_head phase holds at most 4 supergroups per warp
+  std::vector<MegaPhase> prog;
+  size_t smem_f = 64;  // floats
+  auto wred_f = [&]() { return (size_t)kMegaWarps * 2 * NB * 32; };
+  auto note_full = [&](int K, int r_parts) { smem_f = std::max(smem_f, (size_t)(2 + r_parts) * NB * K + 32 * NB + wred_f()); };
+  auto note_slice = [&](const MegaPhase& ph) {
+    const int sgk = ph.fmt == FMT_W4A16 ? 256 : 64;
+    smem_f = std::max(smem_f, (size_t)ph.upc * NB * ph.spu * sgk + wred_f());
+  };
+  // K-slice partial buffers for the branches summed by the next residual update
+  float *o_parts = nullptr, *d_parts = nullptr, *pmp_parts = nullptr;
+  TRY(dalloc(h, &o_parts, (size_t)8 * NB * H));
+  TRY(dalloc(h, &d_parts, (size_t)8 * NB * H));
+  TRY(dalloc(h, &pmp_parts, (size_t)8 * NB * L * P));
+  float* cur = h->x0;
+  auto next_x = [&]() { return cur == h->xb[0] ? h->xb[1] : h->xb[0]; };
+  {  // PMP: pr = W_pmp (E[t] sqrt H), K-slice partials
+    MegaPhase ph{};
+    ph.type = PH_PMP;
+    mega_lin(ph, h->pmp);
+    mega_plan(h->pmp, G, true, ph);
+    ph.in_mode = IN_EMBED;
+    ph.x_stride = H;
+    ph.y = pmp_parts;
+    ph.y_stride = L * P;
+    ph.y_part_stride = (long)NB * L * P;
+    ph.epi = EPI_STORE;
+    note_full(H, 0);
+    prog.push_back(ph);
+    MegaPhase pl{};
+    pl.type = PH_PLE;
+    pl.L = L;
+    pl.P = P;
+    pl.pr_parts = pmp_parts;
+    pl.pr_nparts = ph.ksplit;
+    pl.pr_part_stride = ph.y_part_stride;
+    pl.g_ppn = h->g_ppn;
+    pl.ple_table = h->ple_table;
+    pl.ple_out = h->ple;
+    pl.inv_sqrt_h = (float)(1.0 / std::sqrt((double)H));
+    pl.inv_sqrt2 = (float)(1.0 / std::sqrt(2.0));
+    pl.sqrt_p = (float)std::sqrt((double)P);
+    smem_f = std::max(smem_f, (size_t)P + 64);
+    prog.push_back(pl);
+  }
+  int prev_parts = 1;              // r_ple comes as one final vector
+  for (int l = 0; l < L; ++l) {
+    const Layer& Y = h->layers[l];
+    const int nqd = nq * Y.d;
+    {  // QKV (final rows: attention reads them)
+      MegaPhase ph{};
+      ph.type = PH_GEMV;
+      mega_lin(ph, Y.qkv);
+      mega_plan(Y.qkv, G, false, ph);
+      ph.x_stride = H;
+      ph.g_a = Y.in_norm;
+      if (l == 0) {
+        ph.in_mode = IN_EMBED_NORM;
+        ph.x_out = h->x0;
+        note_full(H, 0);
+      } else {
+        const Layer& Pv = h->layers[l - 1];
+        ph.in_mode = IN_RESID;
+        ph.x_in = cur;
+        ph.r_in = h->r_ple;
+        ph.r_parts = prev_parts;
+        ph.r_part_stride = 0;
+        ph.r_stride = H;
+        ph.g_r = Pv.post_ple_norm;
+        ph.lambda = Pv.lambda;
+        ph.x_out = next_x();
+        cur = ph.x_out;
+        note_full(H, prev_parts);
+      }
+      ph.y = h->qkv;
+      ph.y_stride = Y.qkv.n_valid;
+      ph.epi = EPI_STORE;
+      prog.push_back(ph);
+    }
+    {  // attention
+      const Layer& Src = h->layers[Y.src];
+      MegaPhase ph{};
+      ph.type = PH_ATTN;
+      AttnArgs& a = ph.attn;
+      a.qkv = h->qkv;
+      a.qkv_stride = Y.qkv.n_valid;
+      a.nq = nq;
+      a.g_q = Y.q_norm;
+      a.g_k = Y.k_norm;
+      a.eps = c.rms_eps;
+      a.scale = Y.scale;
+      a.window = Y.full ? 0 : c.sliding_window;
+      a.own = Y.own;
+      a.kc = h->kc[Src.kv];
+      a.vc = h->vc[Src.kv];
+      a.t_max = c.max_context;
+      a.max_batch = c.max_batch;
+      a.rope_cos = h->cos_t[Y.full];
+      a.rope_sin = h->sin_t[Y.full];
+      a.out = h->attn;
+      a.out_stride = nqd;
+      const int max_keys = Y.full ? c.max_context : std::min(c.sliding_window, c.max_context);
+      a.nsplit = attn_nsplit(h->sms, nq, 1, 1, max_keys);
+      a.nstage = 1;
+      a.ws_ml = h->attn_ml;
+      a.ws_o = h->attn_o;
+      a.counters = h->attn_cnt;
+      a.err = h->err;
+      ph.attn_d = Y.d;
+      ph.attn_hpc = 1;
+      ph.attn_units = NB * nq * a.nsplit;
+      if ((size_t)NB * nq * a.nsplit * 2 > h->attn_ml_n || (size_t)NB * nq * a.nsplit * Y.d > h->attn_o_n)
+        return G4_OK;  // workspace sized for another plan: keep the launch-per-phase path
+      size_t ab = 0;
+      switch (Y.d) {
+        case 64: ab = attn_smem_bytes<64, 1>(1); break;
+        case 128: ab = attn_smem_bytes<128, 1>(1); break;
+        case 256: ab = attn_smem_bytes<256, 1>(1); break;
+        default: ab = attn_smem_bytes<512, 1>(1); break;
+      }
+      smem_f = std::max(smem_f, (2 * ab + 3) / 4);
+      prog.push_back(ph);
+    }
+    {  // O: K-slice partials summed by the gate/up residual update
+      MegaPhase ph{};
+      ph.type = PH_GEMV;
+      mega_lin(ph, Y.o);
+      mega_plan(Y.o, G, true, ph);
+      ph.in_mode = IN_PLAIN;
+      ph.x_in = h->attn;
+      ph.x_stride = nqd;
+      ph.y = o_parts;
+      ph.y_stride = H;
+      ph.y_part_stride = (long)NB * H;
+      ph.epi = EPI_STORE;
+      note_slice(ph);
+      prog.push_back(ph);
+      prev_parts = ph.ksplit;
+    }
+    {  // gate/up with GeGLU (final)
+      MegaPhase ph{};
+      ph.type = PH_GEMV;
+      mega_lin(ph, Y.gu);
+      mega_plan(Y.gu, G, false, ph);
+      ph.in_mode = IN_RESID;
+      ph.x_in = cur;
+      ph.x_stride = H;
+      ph.r_in = o_parts;
+      ph.r_parts = prev_parts;
+      ph.r_part_stride = (long)NB * H;
+      ph.r_stride = H;
+      ph.g_r = Y.post_attn_norm;
+      ph.lambda = 1.f;
+      ph.g_a = Y.pre_ffw_norm;
+      ph.x_out = next_x();
+      cur = ph.x_out;
+      ph.y = h->act;
+      ph.y_stride = Y.F;
+      ph.epi = EPI_GEGLU;
+      note_full(H, prev_parts);
+      prog.push_back(ph);
+    }
+    {  // down: partials
+      MegaPhase ph{};
+      ph.type = PH_GEMV;
+      mega_lin(ph, Y.down);
+      mega_plan(Y.down, G, true, ph);
+      ph.in_mode = IN_PLAIN;
+      ph.x_in = h->act;
+      ph.x_stride = Y.F;
+      ph.y = d_parts;
+      ph.y_stride = H;
+      ph.y_part_stride = (long)NB * H;
+      ph.epi = EPI_STORE;
+      note_slice(ph);
+      prog.push_back(ph);
+      prev_parts = ph.ksplit;
+    }
+    {  // PLE gate (final, gelu * ple_l)
+      MegaPhase ph{};
+      ph.type = PH_GEMV;
+      mega_lin(ph, Y.pg);
+      mega_plan(Y.pg, G, false, ph);
+      ph.in_mode = IN_RESID;
+      ph.x_in = cur;
+      ph.x_stride = H;
+      ph.r_in = d_parts;
+      ph.r_parts = prev_parts;
+      ph.r_part_stride = (long)NB * H;
+      ph.r_stride = H;
+      ph.g_r = Y.post_ffw_norm;
+      ph.lambda = 1.f;
+      ph.g_a = nullptr;
+      ph.x_out = next_x();
+      cur = ph.x_out;
+      ph.y = h->pg;
+      ph.y_stride = P;
+      ph.epi = EPI_PLE;
+      ph.ple = h->ple + (size_t)l * P;
+      ph.ple_stride = L * P;
+      note_full(H, prev_parts);
+      prog.push_back(ph);
+    }
+    {  // PLE proj (final r_ple)
+      MegaPhase ph{};
+      ph.type = PH_GEMV;
+      mega_lin(ph, Y.pp);
+      mega_plan(Y.pp, G, false, ph);
+      ph.in_mode = IN_PLAIN;
+      ph.x_in = h->pg;
+      ph.x_stride = P;
+      ph.y = h->r_ple;
+      ph.y_stride = H;
+      ph.epi = EPI_STORE;
+      note_slice(ph);
+      prog.push_back(ph);
+      prev_parts = 1;
+    }
+  }
+  {  // lm_head + argmax
+    const Layer& Pv = h->layers[L - 1];
+    MegaPhase ph{};
+    ph.type = PH_LMHEAD;
+    mega_lin(ph, h->lm);
+    ph.in_mode = IN_RESID;
+    ph.x_in = cur;
+    ph.x_stride = H;
+    ph.r_in = h->r_ple;
+    ph.r_parts = 1;
+    ph.r_stride = H;
+    ph.g_r = Pv.post_ple_norm;
+    ph.lambda = Pv.lambda;
+    ph.g_a = h->g_final;
+    ph.x_out = next_x();
+    note_full(H, 1);
+    prog.push_back(ph);
+    MegaPhase am{};
+    am.type = PH_ARGMAX;
+    prog.push_back(am);
+  }
+  h->mega_smem = smem_f * 4 + 1024;
+  int optin = init_kernel_attrs(h->device);
+  if ((int)h->mega_smem > optin) return G4_OK;
+  int nb1 = 0, nb2 = 0;
+  CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb1, mega_step_kernel<1>, kMegaThreads, h->mega_smem));
+  CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb2, mega_step_kernel<2>, kMegaThreads, h->mega_smem));
+  if (nb1 < 1 || nb2 < 1) return G4_OK;
+  h->mega_grid = G;
+  h->mega_n = (int)prog.size();
+  TRY(dalloc(h, &h->mega_phases, prog.size()));
+  CK(cudaMemcpyAsync(h->mega_phases, prog.data(), prog.size() * sizeof(MegaPhase), cudaMemcpyHostToDevice, st));
+  TRY(dalloc(h, &h->mega_bar, 2));
+  TRY(dalloc(h, &h->mega_am_val, (size_t)NB * G));
+  TRY(dalloc(h, &h->mega_am_idx, (size_t)NB * G));
+  CK(cudaStreamSynchronize(st));
+  h->mega_ok = true;
+  return G4_OK;
+}
+
+g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens,
+                        const int* d_idx, const int* d_pos, int* d_next, float* d_logits) {
+  MegaArgs a{};
+  a.phases = h->mega_phases;
+  a.n_phases = h->mega_n;
+  a.nb = n;
+  a.slots = d_slots;
+  a.positions = d_pos;
+  a.tokens = d_tokens;
+  a.tok_idx = d_idx;
+  a.embed = h->embed;
+  a.H = h->cfg.hidden;
+  a.V = h->cfg.vocab;
+  a.sqrt_h = (float)std::sqrt((double)h->cfg.hidden);
+  a.eps = h->cfg.rms_eps;
+  a.barrier = h->mega_bar;
+  a.am_val = h->mega_am_val;
+  a.am_idx = h->mega_am_idx;
+  a.next_ids = d_next;
+  a.logits = d_logits;
+  a.logits_stride = h->cfg.vocab;
+  a.err = h->err;
+  CK(cudaMemsetAsync(h->mega_bar, 0, 2 * sizeof(unsigned), st));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(h->mega_grid);
+  cfg.blockDim = dim3(kMegaThreads);
+  cfg.dynamicSmemBytes = h->mega_smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (n == 1) CK(cudaLaunchKernelEx(&cfg, mega_step_kernel<1>, a));
+  else CK(cudaLaunchKernelEx(&cfg, mega_step_kernel<2>, a));
+  return G4_OK;
+}
+
 bool is_pow2_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
 g4_status validate(const g4_config* c) {
@@ -955,6 +1322,7 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   TRY(dalloc(h, &h->step_next, B));
   TRY(dalloc(h, &h->step_logits, (size_t)B * c.vocab));
   CK(cudaStreamSynchronize(st));
+  if (mega_enabled()) TRY(build_mega(h, st));
   return G4_OK;
 }
 
