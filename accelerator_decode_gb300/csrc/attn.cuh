@@ -84,8 +84,8 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   const int h0 = hg * HPC;
   const int n_hg = a.nq / HPC;
 
-  int p = a.positions[b];
-  const int slot = a.slots[b];
+  int p = __ldcg(a.positions + b);
+  const int slot = __ldcg(a.slots + b);
   bool bad = false;
   if (p < 0 || p >= a.t_max) { if (split == 0 && hg == 0 && tid == 0) set_err(a.err, G4_DEV_BAD_POSITION); bad = true; }
   if (slot < 0 || slot >= a.max_batch) { if (split == 0 && hg == 0 && tid == 0) set_err(a.err, G4_DEV_BAD_SLOT); bad = true; }
@@ -124,7 +124,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
       const float* src = qraw + (size_t)(h0 + hh) * D;
       float qv[D / 32];
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) qv[e] = src[lane + 32 * e];
+      for (int e = 0; e < D / 32; ++e) qv[e] = __ldcg(src + lane + 32 * e);  // written by another grid/CTA
       float ss = 0.f;
 #pragma unroll
       for (int e = 0; e < D / 32; ++e) ss += qv[e] * qv[e];
@@ -150,7 +150,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
     const float* vr = kr + D;
     float kv_[D / 32];
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) kv_[e] = kr[lane + 32 * e];
+    for (int e = 0; e < D / 32; ++e) kv_[e] = __ldcg(kr + lane + 32 * e);
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < D / 32; ++e) ss += kv_[e] * kv_[e];
@@ -174,7 +174,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
     }
 #pragma unroll
     for (int e = 0; e < D / 32; ++e) {
-      const __nv_bfloat16 v1 = __float2bfloat16_rn(vr[lane + 32 * e]);
+      const __nv_bfloat16 v1 = __float2bfloat16_rn(__ldcg(vr + lane + 32 * e));
       vnew[lane + 32 * e] = bf16f(v1);
       if (hg == 0) vdst[lane + 32 * e] = v1;
     }

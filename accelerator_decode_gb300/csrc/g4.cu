@@ -79,11 +79,11 @@ struct Layer {
 };
 
 struct GraphKey {
-  int n;
+  int n, mode;
   const void *slots, *tokens, *pos, *next, *logits, *trace;
   bool operator<(const GraphKey& o) const {
-    return std::tie(n, slots, tokens, pos, next, logits, trace) <
-           std::tie(o.n, o.slots, o.tokens, o.pos, o.next, o.logits, o.trace);
+    return std::tie(n, mode, slots, tokens, pos, next, logits, trace) <
+           std::tie(o.n, o.mode, o.slots, o.tokens, o.pos, o.next, o.logits, o.trace);
   }
 };
 
@@ -127,11 +127,14 @@ struct g4_handle {
   float* trace = nullptr;
   int trace_stride = 0;
   // persistent step (n <= 2)
-  bool mega_ok = false;
+  bool mega_ok = false;  // the persistent step was planned for this model
+  bool mega_on = false;  // g4_set_step_mode(1): n_seq <= 2 steps run it
   MegaPhase* mega_phases = nullptr;
   int mega_n = 0, mega_grid = 0;
   size_t mega_smem = 0;
   unsigned* mega_bar = nullptr;
+  unsigned long long* mega_stamps = nullptr;
+  std::vector<std::string> mega_names;  // phase names (profiling)
   float *mega_am_val = nullptr;
   int* mega_am_idx = nullptr;
   // graphs
@@ -563,13 +566,11 @@ struct ProfScope {
 
 // ------------------------------------------------------------------------------- the step
 g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens,
-                        const int* d_idx, const int* d_pos, int* d_next, float* d_logits);
-bool mega_enabled();
-
+                        const int* d_idx, const int* d_pos, int* d_next, float* d_logits, bool stamps);
 g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens, const int* d_idx,
                    const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr) {
-  if (h->mega_ok && mega_enabled() && n <= 2 && !h->trace && !prof)
-    return run_step_mega(h, st, n, d_slots, d_tokens, d_idx, d_pos, d_next, d_logits);
+  if (h->mega_ok && h->mega_on && n <= 2 && !prof)
+    return run_step_mega(h, st, n, d_slots, d_tokens, d_idx, d_pos, d_next, d_logits, false);
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
   const float eps = c.rms_eps;
@@ -781,14 +782,6 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
 }
 
 // ------------------------------------------------------------------- persistent step
-bool mega_enabled() {
-  static const bool on = [] {
-    const char* e = getenv("G4_MEGA");
-    return !(e && e[0] == '0');
-  }();
-  return on;
-}
-
 // Units of one projection phase: K slices of spu supergroups, wpu warps per unit, upc units
 // per CTA at a time.  Minimises rounds x supergroups per warp; ties go to fewer K slices.
 void mega_plan(const Lin& L, int G, bool allow_split, MegaPhase& ph) {
@@ -1073,6 +1066,33 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
     am.type = PH_ARGMAX;
     prog.push_back(am);
   }
+  {
+    static const char* kLayerNames[] = {"mega.qkv", "mega.attn", "mega.o", "mega.gate_up", "mega.down",
+                                        "mega.ple_gate", "mega.ple_proj"};
+    h->mega_names.clear();
+    h->mega_names.push_back("mega.ple_model_proj");
+    h->mega_names.push_back("mega.ple_combine");
+    for (int l = 0; l < L; ++l)
+      for (const char* nm : kLayerNames) h->mega_names.push_back(nm);
+    h->mega_names.push_back("mega.lm_head");
+    h->mega_names.push_back("mega.argmax");
+  }
+  // per-layer trace points: residual after layer l is materialised by layer l+1's QKV phase
+  // (the lm_head phase for the last layer); attention output of layer l is read by its O phase
+  {
+    for (MegaPhase& ph : prog) {
+      ph.trace_x = -1;
+      ph.trace_attn = -1;
+    }
+    int idx = 2;
+    for (int l = 0; l < L; ++l) {
+      if (l > 0) prog[idx].trace_x = l - 1;      // QKV of layer l
+      prog[idx + 2].trace_attn = l;               // O of layer l
+      prog[idx + 2].trace_attn_width = nq * h->layers[l].d;
+      idx += 7;
+    }
+    prog[idx].trace_x = L - 1;                    // lm_head
+  }
   h->mega_smem = smem_f * 4 + 1024;
   int optin = init_kernel_attrs(h->device);
   if ((int)h->mega_smem > optin) return G4_OK;
@@ -1082,6 +1102,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
   if (nb1 < 1 || nb2 < 1) return G4_OK;
   h->mega_grid = G;
   h->mega_n = (int)prog.size();
+  TRY(dalloc(h, &h->mega_stamps, prog.size() + 1));
   TRY(dalloc(h, &h->mega_phases, prog.size()));
   CK(cudaMemcpyAsync(h->mega_phases, prog.data(), prog.size() * sizeof(MegaPhase), cudaMemcpyHostToDevice, st));
   TRY(dalloc(h, &h->mega_bar, 2));
@@ -1093,8 +1114,9 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
 }
 
 g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens,
-                        const int* d_idx, const int* d_pos, int* d_next, float* d_logits) {
+                        const int* d_idx, const int* d_pos, int* d_next, float* d_logits, bool stamps) {
   MegaArgs a{};
+  a.stamps = stamps ? h->mega_stamps : nullptr;
   a.phases = h->mega_phases;
   a.n_phases = h->mega_n;
   a.nb = n;
@@ -1114,6 +1136,9 @@ g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots
   a.logits = d_logits;
   a.logits_stride = h->cfg.vocab;
   a.err = h->err;
+  a.trace = h->trace;
+  a.trace_stride = h->trace_stride;
+  a.max_batch = h->cfg.max_batch;
   CK(cudaMemsetAsync(h->mega_bar, 0, 2 * sizeof(unsigned), st));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h->mega_grid);
@@ -1301,28 +1326,29 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   TRY(dalloc(h, &h->am_idx, h->am_n));
   // attention scratch for the largest (nb * nsplit) over batch sizes
   size_t ml = 1, ao = 1;
-  for (int nb = 1; nb <= B; ++nb) {
+  for (int nb = 1; nb <= std::max(B, 2); ++nb) {  // the persistent step plans for 2 rows
     const int hpc = attn_hpc(nq, nb);
     for (int t = 0; t < 2; ++t) {
       const int d = t ? c.head_dim_full : c.head_dim_sliding;
       const int keys = t ? c.max_context : std::min(c.sliding_window, c.max_context);
       const int ns = attn_nsplit(h->sms, nq, hpc, nb, keys);
-      ml = std::max(ml, (size_t)nb * nq * ns * 2);
-      ao = std::max(ao, (size_t)nb * nq * ns * d);
+      const int ns1 = attn_nsplit(h->sms, nq, 1, 1, keys);  // persistent step: nb=1 plan, 2 rows
+      ml = std::max({ml, (size_t)nb * nq * ns * 2, (size_t)2 * nq * ns1 * 2});
+      ao = std::max({ao, (size_t)nb * nq * ns * d, (size_t)2 * nq * ns1 * d});
     }
   }
   h->attn_ml_n = ml;
   h->attn_o_n = ao;
   TRY(dalloc(h, &h->attn_ml, ml));
   TRY(dalloc(h, &h->attn_o, ao));
-  TRY(dalloc(h, &h->attn_cnt, (size_t)B * nq));
-  CK(cudaMemsetAsync(h->attn_cnt, 0, (size_t)B * nq * sizeof(unsigned), st));
+  TRY(dalloc(h, &h->attn_cnt, (size_t)std::max(B, 2) * nq));
+  CK(cudaMemsetAsync(h->attn_cnt, 0, (size_t)std::max(B, 2) * nq * sizeof(unsigned), st));
   TRY(dalloc(h, &h->err, 1));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), st));
   TRY(dalloc(h, &h->step_next, B));
   TRY(dalloc(h, &h->step_logits, (size_t)B * c.vocab));
   CK(cudaStreamSynchronize(st));
-  if (mega_enabled()) TRY(build_mega(h, st));
+  TRY(build_mega(h, st));
   return G4_OK;
 }
 
@@ -1386,6 +1412,18 @@ void g4_free(g4_handle* h) {
 
 int64_t g4_device_bytes(const g4_handle* h) { return h ? (int64_t)h->bytes : 0; }
 
+int32_t g4_step_mode(const g4_handle* h, int32_t n_seq) {
+  if (!h) return -1;
+  return (h->mega_ok && h->mega_on && n_seq <= 2) ? 1 : 0;
+}
+
+g4_status g4_set_step_mode(g4_handle* h, int32_t mode) {
+  if (!h || (mode != 0 && mode != 1)) return G4_ERR_INVALID_ARG;
+  if (mode == 1 && !h->mega_ok) return G4_ERR_UNSUPPORTED;
+  h->mega_on = mode == 1;
+  return G4_OK;
+}
+
 g4_status g4_set_trace(g4_handle* h, float* d_trace, int64_t capacity_floats) {
   if (!h) return G4_ERR_INVALID_ARG;
   const g4_config& c = h->cfg;
@@ -1405,7 +1443,7 @@ g4_status g4_decode_step(g4_handle* h, g4_stream stream, int32_t n_seq, const in
   if (st == nullptr) {  // the legacy default stream cannot be captured: launch directly
     return run_step(h, st, n_seq, d_slots, d_tokens, nullptr, d_positions, d_next_ids, d_logits);
   }
-  GraphKey key{n_seq, d_slots, d_tokens, d_positions, d_next_ids, d_logits, h->trace};
+  GraphKey key{n_seq, g4_step_mode(h, n_seq), d_slots, d_tokens, d_positions, d_next_ids, d_logits, h->trace};
   auto it = h->graphs.find(key);
   if (it == h->graphs.end()) {
     if (h->graphs.size() >= 16) {
@@ -1497,6 +1535,37 @@ g4_status g4_profile_step(g4_handle* h, g4_stream stream, int32_t n_seq, const i
   if (n_seq < 1 || n_seq > h->cfg.max_batch) return G4_ERR_INVALID_ARG;
   CK(cudaSetDevice(h->device));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (h->mega_ok && h->mega_on && n_seq <= 2) {
+    // persistent step: per-phase durations from the %globaltimer stamps CTA 0 takes after
+    // every grid barrier (phase k ends when barrier k releases)
+    std::map<std::string, g4_phase_stat> agg;
+    std::vector<std::string> order;
+    std::vector<unsigned long long> ts(h->mega_n + 1);
+    for (int r = 0; r < repeats; ++r) {
+      TRY(run_step_mega(h, st, n_seq, d_slots, d_tokens, nullptr, d_positions, d_next_ids, d_logits, true));
+      CK(cudaMemcpyAsync(ts.data(), h->mega_stamps, ts.size() * 8, cudaMemcpyDeviceToHost, st));
+      CK(cudaStreamSynchronize(st));
+      for (int p = 0; p < h->mega_n; ++p) {
+        const std::string& nm = h->mega_names[p];
+        auto it = agg.find(nm);
+        if (it == agg.end()) {
+          g4_phase_stat z{};
+          snprintf(z.name, sizeof z.name, "%s", nm.c_str());
+          it = agg.emplace(nm, z).first;
+          order.push_back(nm);
+        }
+        it->second.launches += 1;
+        it->second.ms_total += (double)(ts[p + 1] - ts[p]) * 1e-6;
+      }
+    }
+    int k = 0;
+    for (const std::string& nm : order) {
+      if (k >= max_stats) break;
+      stats[k++] = agg[nm];
+    }
+    *n_stats = k;
+    return G4_OK;
+  }
   Prof prof;
   prof.st = st;
   float* saved_trace = h->trace;

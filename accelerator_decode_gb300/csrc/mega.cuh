@@ -18,6 +18,8 @@
 // at once with wpu warps each (upc * wpu = 8).  The grid barrier is a monotonically
 // increasing counter (cleared before the launch); its wait is bounded: on expiry a CTA sets
 // the timeout bit and the abort flag, and every CTA leaves at its next barrier.
+// Visibility: data written by other CTAs earlier in the launch is read only through L2 (cp.async.cg,
+// ld.global.cg) or after the barrier's acquire fence, never from a possibly stale L1 line.
 #pragma once
 #include "attn.cuh"
 #include "common.cuh"
@@ -51,6 +53,9 @@ struct MegaPhase {
   float lambda;
   const __nv_bfloat16* g_a;
   float* x_out;            // IN_RESID / IN_EMBED*: the new residual (CTA 0 writes it)
+  int trace_x;             // >= 0: the new residual is the stream after layer trace_x
+  int trace_attn;          // >= 0: copy the attention output of layer trace_attn (IN_PLAIN phase)
+  int trace_attn_width;
   // output
   float* y;
   int y_stride;
@@ -90,7 +95,16 @@ struct MegaArgs {
   float* logits;
   int logits_stride;
   int* err;
+  unsigned long long* stamps;  // optional [n_phases + 1] %globaltimer after each phase (CTA 0)
+  float* trace;                // optional per-layer trace (layout of g4_set_trace)
+  int trace_stride, max_batch;
 };
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
@@ -122,6 +136,7 @@ __device__ __forceinline__ bool grid_sync(const MegaArgs& a, unsigned k, int* ab
       }
       __nanosleep(64);
     }
+    __threadfence();  // acquire side: later reads of this CTA see every CTA's phase writes
     *abort_s = ab;
   }
   __syncthreads();
@@ -197,6 +212,9 @@ __device__ void mega_full_input(const MegaArgs& a, const MegaPhase& ph, float* x
       const int b = i / c4, c = i - b * c4;
       *reinterpret_cast<float4*>(ph.x_out + (size_t)b * ph.x_stride + 4 * c) =
           *reinterpret_cast<const float4*>(xf + b * K + 4 * c);
+      if (a.trace && ph.trace_x >= 0)
+        *reinterpret_cast<float4*>(a.trace + ((size_t)(ph.trace_x * 2 + 1) * a.max_batch + b) * a.trace_stride + 4 * c) =
+            *reinterpret_cast<const float4*>(xf + b * K + 4 * c);
     }
   }
   if (ph.in_mode != IN_EMBED && ph.g_a != nullptr) {
@@ -230,6 +248,12 @@ __device__ void mega_gemv(const MegaArgs& a, const MegaPhase& ph, float* smem) {
   float* xsl = smem;
   float* wred = full_in ? red + 32 * NB : xsl + ph.upc * NB * slice;  // [8][2 * NB * 32]
   if (full_in) mega_full_input<NB>(a, ph, xf, rf, red);
+  if (a.trace && ph.trace_attn >= 0 && blockIdx.x == 0) {
+    for (int b = 0; b < a.nb; ++b)
+      for (int k = threadIdx.x; k < ph.trace_attn_width; k += blockDim.x)
+        a.trace[((size_t)(ph.trace_attn * 2) * a.max_batch + b) * a.trace_stride + k] =
+            __ldcg(ph.x_in + (size_t)b * ph.x_stride + k);
+  }
   const int slot = warp / ph.wpu, wi = warp % ph.wpu;
   const int n_batches = (ph.n_units + ph.upc - 1) / ph.upc;
   for (int bt = blockIdx.x; bt < n_batches; bt += gridDim.x) {
@@ -323,7 +347,7 @@ __device__ void mega_gemv(const MegaArgs& a, const MegaPhase& ph, float* smem) {
               if (n < ph.n_valid) ph.y[(size_t)b * ph.y_stride + n] = gelu_tanh(g) * v;
             }
           } else if (row < ph.n_valid) {
-            if (ph.epi == EPI_PLE) v = gelu_tanh(v) * ph.ple[(size_t)b * ph.ple_stride + row];
+            if (ph.epi == EPI_PLE) v = gelu_tanh(v) * __ldcg(ph.ple + (size_t)b * ph.ple_stride + row);
             ph.y[(size_t)b * ph.y_stride + row] = v;
           }
         }
@@ -346,7 +370,7 @@ __device__ void mega_ple(const MegaArgs& a, const MegaPhase& ph, float* smem) {
     for (int i = tid; i < ph.P; i += nt) {
       float x = 0.f;
       for (int s = 0; s < ph.pr_nparts; ++s)
-        x += ph.pr_parts[s * ph.pr_part_stride + (size_t)b * ph.L * ph.P + l * ph.P + i];
+        x += __ldcg(ph.pr_parts + s * ph.pr_part_stride + (size_t)b * ph.L * ph.P + l * ph.P + i);
       x *= ph.inv_sqrt_h;
       v[i] = x;
       ss[0] += x * x;
@@ -487,6 +511,7 @@ __global__ void __launch_bounds__(kMegaThreads, 1) mega_step_kernel(const MegaAr
     const int t = a.tok_idx ? a.tokens[a.tok_idx[threadIdx.x]] : a.tokens[threadIdx.x];
     if (t < 0 || t >= a.V) set_err(a.err, G4_DEV_BAD_TOKEN);
   }
+  if (a.stamps && blockIdx.x == 0 && threadIdx.x == 0) a.stamps[0] = globaltimer_ns();
   for (int p = 0; p < a.n_phases; ++p) {
     const MegaPhase& ph = a.phases[p];
     switch (ph.type) {
@@ -514,6 +539,7 @@ __global__ void __launch_bounds__(kMegaThreads, 1) mega_step_kernel(const MegaAr
         break;
     }
     if (p + 1 < a.n_phases && !grid_sync(a, (unsigned)p, &abort_s)) return;
+    if (a.stamps && blockIdx.x == 0 && threadIdx.x == 0) a.stamps[p + 1] = globaltimer_ns();
   }
 }
 

@@ -85,6 +85,8 @@ def _load():
         "g4_get_device_error": (c_int, [P, P, POINTER(c_int32)]),
         "g4_set_trace": (c_int, [P, P, c_int64]),
         "g4_device_bytes": (c_int64, [P]),
+        "g4_step_mode": (c_int32, [P, c_int32]),
+        "g4_set_step_mode": (c_int, [P, c_int32]),
         "g4_profile_step": (c_int, [P, P, c_int32, P, P, P, P, P, c_int32, POINTER(g4_phase_stat), c_int32,
                                     POINTER(c_int32)]),
         "g4_free": (None, [P]),
@@ -159,6 +161,10 @@ def g4_get_device_error(h, stream):
     w = c_int32(0)
     s = lib.g4_get_device_error(h, stream, ctypes.byref(w))
     return s, w.value
+
+
+def g4_set_step_mode(h, mode):
+    check(lib.g4_set_step_mode(h, mode), "g4_set_step_mode")
 
 
 def g4_set_trace(h, d_trace, capacity):

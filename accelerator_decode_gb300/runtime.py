@@ -118,6 +118,14 @@ class Decoder:
             self._trace = None
         return self._trace
 
+    def step_mode(self, n_seq=1):
+        """1: persistent single-launch step; 0: one launch per phase."""
+        return _g4.lib.g4_step_mode(self.h, n_seq)
+
+    def set_step_mode(self, mode):
+        """0 (default): one launch per phase; 1: persistent single-launch step for n_seq <= 2."""
+        _g4.g4_set_step_mode(self.h, int(mode))
+
     def device_bytes(self):
         return _g4.lib.g4_device_bytes(self.h)
 

@@ -179,6 +179,19 @@ g4_status g4_profile_step(g4_handle* h, g4_stream stream, int32_t n_seq, const i
 /* Bytes of device memory the handle owns (weights copies, KV cache, workspaces). */
 int64_t g4_device_bytes(const g4_handle* h);
 
+/* Which implementation a step of n_seq sequences runs: 1 = the persistent single-launch step
+ * (selected with g4_set_step_mode and n_seq <= 2), 0 = one launch per phase (replayed as a
+ * CUDA graph), -1 = NULL handle. */
+int32_t g4_step_mode(const g4_handle* h, int32_t n_seq);
+
+/* Select the implementation of steps with n_seq <= 2: mode 0 (the default) launches one kernel
+ * per phase; mode 1 runs the whole step as one persistent cooperative kernel (phases separated
+ * by a bounded grid barrier).  Both compute the same step; their fp32 sums are ordered
+ * differently.  Not thread-safe against concurrent steps on the same handle.  Errors:
+ * G4_ERR_INVALID_ARG (NULL handle, mode not 0/1), G4_ERR_UNSUPPORTED (mode 1 on a model the
+ * persistent step was not planned for, e.g. an lm_head input wider than 2048). */
+g4_status g4_set_step_mode(g4_handle* h, int32_t mode);
+
 /* Release everything the handle owns (after synchronising its device).  NULL is a no-op. */
 void g4_free(g4_handle* h);
 

@@ -5,7 +5,8 @@ Draws (the synthetic workloads' recipe):
     embedding table): N(0, std) drawn in fp32, rounded to bf16 round-to-nearest-even.
   * W4A16 linears: q ~ uniform integers in [-8, 7]; scale = bf16(|N(0, scale_std)|), one per
     32 input values; packed eight nibbles per int32, low nibble first.
-  * RMSNorm gains: bf16(1 + N(0, gain_std)), i.e. exactly 1 at gain_std = 0.
+  * RMSNorm gains: bf16(1 + N(0, gain_std)), i.e. exactly 1 at gain_std = 0; the query and
+    key norms' gains are bf16(qk_gain * that) (qk_gain = 1 leaves them unchanged).
   * layer scales: 1 + N(0, layer_scale_std) in fp32 (exactly 1 at std 0).
 
 Each tensor has its own stream, SeedSequence([seed, tensor id, chunk]), so tensors are
@@ -66,6 +67,12 @@ def _gain_bf16(n, std, seed, tid, pool):
     return bf16_from_f32(np.float32(1.0) + g.view(np.float32))
 
 
+def _scaled_gain(g, factor):
+    if factor == 1.0:
+        return g
+    return bf16_from_f32(np.float32(factor) * (g.astype(np.uint32) << np.uint32(16)).view(np.float32))
+
+
 def _int4_linear(n_out, n_in, scale_std, seed, tid, pool):
     assert n_in % 32 == 0
     q = np.empty(n_out * n_in, np.int8)
@@ -100,13 +107,14 @@ def linear_shapes(cfg, layer):
 
 
 def make_weights(cfg, fmt, seed=0, std=0.02, scale_std=0.004, gain_std=0.0,
-                 layer_scale_std=0.0, embed_std=None):
+                 layer_scale_std=0.0, embed_std=None, qk_gain=1.0):
     """Draw every tensor of the synthetic checkpoint.
 
     fmt: "bf16" (every linear bf16) or "w4a16" (linears int4 + bf16 group scales; the token
     embedding and per-layer-embedding table stay bf16).  K and V projections are drawn for
     every layer, as a checkpoint that carries them everywhere would; a decoder reads those
-    of the layers that compute their own K/V.
+    of the layers that compute their own K/V.  qk_gain < 1 softens the attention scores
+    (they scale with qk_gain squared), which keeps deep random models well conditioned.
     """
     assert fmt in ("bf16", "w4a16")
     L, H, P, V = cfg["num_layers"], cfg["hidden"], cfg["ple_dim"], cfg["vocab"]
@@ -134,8 +142,8 @@ def make_weights(cfg, fmt, seed=0, std=0.02, scale_std=0.004, gain_std=0.0,
             for i, name in enumerate(_LAYER_NORMS):
                 lw[name] = _gain_bf16(H, gain_std, seed, base + 20 + i, pool)
             d = shapes["k"][0]
-            lw["q_norm"] = _gain_bf16(d, gain_std, seed, base + 30, pool)
-            lw["k_norm"] = _gain_bf16(d, gain_std, seed, base + 31, pool)
+            lw["q_norm"] = _scaled_gain(_gain_bf16(d, gain_std, seed, base + 30, pool), qk_gain)
+            lw["k_norm"] = _scaled_gain(_gain_bf16(d, gain_std, seed, base + 31, pool), qk_gain)
             if layer_scale_std == 0.0:
                 lw["layer_scale"] = 1.0
             else:

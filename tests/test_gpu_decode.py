@@ -78,13 +78,18 @@ def check_parity(ref, toks, logits, label):
 CASES = [("tiny", "bf16"), ("tiny", "w4a16"), ("tiny10", "bf16"), ("tiny10", "w4a16")]
 
 
+@pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("name,fmt", CASES)
-def test_tiny_greedy_matches_oracle(rt, name, fmt):
+def test_tiny_greedy_matches_oracle(rt, name, fmt, mode):
+    """mode 0: one launch per phase (CUDA graph); mode 1: the persistent single-launch step."""
     cfg = synth.get_config(name)
     w = synth.make_weights(cfg, fmt, seed=0, gain_std=0.1, layer_scale_std=0.05)
     prompts = synth.make_prompts(cfg["vocab"], 1, 16, seed=0)
     ref = oracle.Oracle(cfg, w, max_batch=1, max_context=64).generate(prompts, 16, keep_logits=True)
     dec = rt.Decoder(cfg, w, max_batch=1, max_context=64)
+    assert dec.step_mode(1) == 0, "launch per phase is the default"
+    dec.set_step_mode(mode)
+    assert dec.step_mode(1) == mode
     toks, logits = gpu_generate(dec, list(prompts), 16)
     assert dec.device_error()[1] == 0
     dec.close()
@@ -252,3 +257,36 @@ def test_batch16_tensor_core_path(rt, fmt):
         assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL
         ok = ref["gaps"].T > GAP_TIE
         assert np.all((toks == ref["tokens"]) | ~ok)
+
+
+def test_persistent_step_two_sequences_matches_oracle(rt):
+    """The persistent step with two sequences at different positions (ragged prompts), with a
+    per-layer trace set, against the oracle; a third sequence falls back to one launch per
+    phase within the same handle."""
+    cfg = synth.get_config("tiny10")
+    w = synth.make_weights(cfg, "w4a16", seed=21, gain_std=0.1)
+    dec = rt.Decoder(cfg, w, max_batch=3, max_context=32)
+    dec.set_step_mode(1)
+    assert dec.step_mode(2) == 1 and dec.step_mode(3) == 0
+    dec.set_trace(True)
+    for n in (2, 3):
+        prompts = synth.make_prompts(cfg["vocab"], n, 10, seed=2 + n)
+        ref = oracle.Oracle(cfg, w, max_batch=n, max_context=32).generate(prompts, 6, keep_logits=True)
+        toks, logits = gpu_generate(dec, list(prompts), 6, teacher=ref["tokens"])
+        assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL, n
+        ok = ref["gaps"].T > GAP_TIE
+        assert np.all((toks == ref["tokens"]) | ~ok)
+    assert dec.device_error()[1] == 0
+    dec.close()
+
+
+def test_step_mode_argument_checks(rt):
+    from accelerator_decode_gb300 import g4
+    cfg = synth.get_config("tiny")
+    dec = rt.Decoder(cfg, synth.make_weights(cfg, "w4a16", seed=1), max_batch=1, max_context=16)
+    with pytest.raises(g4.G4Error):
+        dec.set_step_mode(2)
+    dec.set_step_mode(1)
+    dec.set_step_mode(0)
+    assert dec.step_mode(1) == 0
+    dec.close()

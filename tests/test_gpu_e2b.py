@@ -23,13 +23,24 @@ def rt():
     return runtime
 
 
+# With unit q/k-norm gains this random 35-layer model is chaotic after ~18 prompt tokens:
+# rounding noise grows through the layers until the fp32 oracle itself differs from the
+# fp64 oracle by 2.6e-2 in the logits, so no fp32 implementation could be held to the
+# tolerance.  q/k gains of 0.5 soften the attention scores (x1/4) and bring that
+# fp32-vs-fp64 difference down to ~2e-6 over the same 24 + 8 tokens.
+QK_GAIN = 0.5
+
+
+@pytest.mark.parametrize("mode", [0, 1])
 @pytest.mark.parametrize("fmt", ["w4a16", "bf16"])
-def test_e2b_short_decode(rt, fmt):
+def test_e2b_short_decode(rt, fmt, mode):
     cfg = synth.get_config("e2b")
-    w = synth.make_weights(cfg, fmt, seed=0)
+    w = synth.make_weights(cfg, fmt, seed=0, qk_gain=QK_GAIN)
     prompts = synth.make_prompts(cfg["vocab"], 1, 24, seed=0)
     ref = oracle.Oracle(cfg, w, max_batch=1, max_context=64).generate(prompts, 8, keep_logits=True)
     dec = rt.Decoder(cfg, w, max_batch=1, max_context=64)
+    dec.set_step_mode(mode)
+    assert dec.step_mode(1) == mode
     toks, logits = gpu_generate(dec, list(prompts), 8, teacher=ref["tokens"])
     assert dec.device_error()[1] == 0
     dec.close()
