@@ -117,9 +117,27 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   if (ntiles > 0) load_tile(0);
   if (ntiles > 1 && a.nstage > 1) load_tile(1);
 
-  // ---- q: per-head RMSNorm then RoPE at position p
+  // ---- q: per-head RMSNorm then RoPE at position p, in registers.  Every global value is
+  // loaded before the first shared-memory store: a load issued after a store through another
+  // pointer may not be moved above it, which would serialise one L2 round trip per element.
+  // RoPE pairs element i with i + D/2; for i = lane + 32 e (e < D/64) the partner is
+  // lane + 32 (e + D/64), so both halves of a pair sit in the same lane.
   const float* qraw = a.qkv + (size_t)b * a.qkv_stride;
+  const bool use_new = a.own && has_p;
+  constexpr int kKvWarp = kAttnThreads / 32 - 1;  // computes the new K/V row beside the q warps
+  float cs[D / 64], sn[D / 64];
+  if (ntiles > 0 || use_new) {
+    const size_t rp = (size_t)(p < 0 ? 0 : p) * (D / 2);
+#pragma unroll
+    for (int e = 0; e < D / 64; ++e) {
+      cs[e] = __ldg(a.rope_cos + rp + lane + 32 * e);
+      sn[e] = __ldg(a.rope_sin + rp + lane + 32 * e);
+    }
+  }
   if (ntiles > 0) {
+    float gq[D / 32];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) gq[e] = bf16f(a.g_q[lane + 32 * e]);
     for (int hh = warp; hh < HPC; hh += kAttnThreads / 32) {
       const float* src = qraw + (size_t)(h0 + hh) * D;
       float qv[D / 32];
@@ -131,50 +149,50 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
       ss = warp_sum(ss);
       const float den = rms_denom(ss, D, a.eps);
 #pragma unroll
-      for (int e = 0; e < D / 32; ++e) qs[hh * D + lane + 32 * e] = (qv[e] / den) * bf16f(a.g_q[lane + 32 * e]);
-      __syncwarp();
+      for (int e = 0; e < D / 32; ++e) qv[e] = (qv[e] / den) * gq[e];
 #pragma unroll
       for (int e = 0; e < D / 64; ++e) {
-        const int i = lane + 32 * e;
-        const float qa = qs[hh * D + i], qb = qs[hh * D + i + D / 2];
-        const float c = a.rope_cos[(size_t)p * (D / 2) + i], s = a.rope_sin[(size_t)p * (D / 2) + i];
-        qs[hh * D + i] = qa * c - qb * s;
-        qs[hh * D + i + D / 2] = qb * c + qa * s;
+        const float qa = qv[e], qb = qv[e + D / 64];
+        qv[e] = qa * cs[e] - qb * sn[e];
+        qv[e + D / 64] = qb * cs[e] + qa * sn[e];
       }
+#pragma unroll
+      for (int e = 0; e < D / 32; ++e) qs[hh * D + lane + 32 * e] = qv[e];
     }
   }
   // ---- new K/V row of an owning layer (position p), computed by every CTA holding key p
-  const bool use_new = a.own && has_p;
-  if (use_new && warp == 0) {
+  if (use_new && warp == kKvWarp) {
     const float* kr = qraw + (size_t)a.nq * D;
     const float* vr = kr + D;
-    float kv_[D / 32];
+    float kv_[D / 32], vv_[D / 32], gk[D / 32];
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) kv_[e] = __ldcg(kr + lane + 32 * e);
+    for (int e = 0; e < D / 32; ++e) {
+      kv_[e] = __ldcg(kr + lane + 32 * e);
+      vv_[e] = __ldcg(vr + lane + 32 * e);
+      gk[e] = bf16f(a.g_k[lane + 32 * e]);
+    }
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < D / 32; ++e) ss += kv_[e] * kv_[e];
     ss = warp_sum(ss);
     const float den = rms_denom(ss, D, a.eps);
 #pragma unroll
-    for (int e = 0; e < D / 32; ++e) knew[lane + 32 * e] = (kv_[e] / den) * bf16f(a.g_k[lane + 32 * e]);
-    __syncwarp();
+    for (int e = 0; e < D / 32; ++e) kv_[e] = (kv_[e] / den) * gk[e];
     __nv_bfloat16* kdst = a.kc + ((size_t)slot * a.t_max + p) * D;
     __nv_bfloat16* vdst = a.vc + ((size_t)slot * a.t_max + p) * D;
 #pragma unroll
     for (int e = 0; e < D / 64; ++e) {
       const int i = lane + 32 * e;
-      const float ka = knew[i], kb = knew[i + D / 2];
-      const float c = a.rope_cos[(size_t)p * (D / 2) + i], s = a.rope_sin[(size_t)p * (D / 2) + i];
-      const __nv_bfloat16 k1 = __float2bfloat16_rn(ka * c - kb * s);
-      const __nv_bfloat16 k2 = __float2bfloat16_rn(kb * c + ka * s);
+      const float ka = kv_[e], kb = kv_[e + D / 64];
+      const __nv_bfloat16 k1 = __float2bfloat16_rn(ka * cs[e] - kb * sn[e]);
+      const __nv_bfloat16 k2 = __float2bfloat16_rn(kb * cs[e] + ka * sn[e]);
       knew[i] = bf16f(k1);
       knew[i + D / 2] = bf16f(k2);
       if (hg == 0) { kdst[i] = k1; kdst[i + D / 2] = k2; }
     }
 #pragma unroll
     for (int e = 0; e < D / 32; ++e) {
-      const __nv_bfloat16 v1 = __float2bfloat16_rn(__ldcg(vr + lane + 32 * e));
+      const __nv_bfloat16 v1 = __float2bfloat16_rn(vv_[e]);
       vnew[lane + 32 * e] = bf16f(v1);
       if (hg == 0) vdst[lane + 32 * e] = v1;
     }

@@ -784,30 +784,26 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
 // ------------------------------------------------------------------- persistent step
 // Units of one projection phase: K slices of spu supergroups, wpu warps per unit, upc units
 // per CTA at a time.  Minimises rounds x supergroups per warp; ties go to fewer K slices.
-void mega_plan(const Lin& L, int G, bool allow_split, MegaPhase& ph) {
+// Persistent-step plan of a projection: K slices (at most max_ks, dividing the supergroups)
+// that balance units of spu supergroups over the G CTAs; ring items of at most kItemMax bytes.
+void mega_plan(const Lin& L, int G, int max_ks, MegaPhase& ph) {
   const int n_rg = L.n_rb / L.R;
   long best_cost = -1;
-  for (int spu = 1; spu <= L.S; ++spu) {
+  for (int spu = L.S; spu >= 1; --spu) {
     if (L.S % spu) continue;
     const int ks = L.S / spu;
-    if ((ks > 1 && !allow_split) || ks > 8) continue;
-    for (int wpu : {8, 4, 2, 1}) {
-      if (wpu > spu && wpu > 1) continue;
-      const int upc = kMegaWarps / wpu;
-      const long units = (long)n_rg * ks;
-      const long rounds = ((units + upc - 1) / upc + G - 1) / G;
-      const long cost = rounds * ((spu + wpu - 1) / wpu);
-      const bool better = best_cost < 0 || cost < best_cost || (cost == best_cost && ks < ph.ksplit);
-      if (better) {
-        best_cost = cost;
-        ph.spu = spu;
-        ph.wpu = wpu;
-        ph.upc = upc;
-        ph.ksplit = ks;
-        ph.n_units = (int)units;
-      }
+    if (ks > max_ks) continue;
+    const long units = (long)n_rg * ks;
+    const long cost = ((units + G - 1) / G) * spu;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      ph.spu = spu;
+      ph.ksplit = ks;
+      ph.n_units = (int)units;
     }
   }
+  const size_t sgb = (size_t)L.R * (8 * kTileBytes + (L.fmt == G4_W4A16 ? kTileBytes : 0));
+  ph.chunk_sg = (int)std::max<size_t>(1, std::min<size_t>(ph.spu, kItemMax / sgb));
 }
 
 void mega_lin(MegaPhase& ph, const Lin& L) {
@@ -826,14 +822,14 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, nq = c.num_q_heads;
   const int G = h->sms, NB = 2;
-  if (h->lm.S > 32 || H % 8) return G4_OK;  // lm_head phase holds at most 4 supergroups per warp
+  if (H % 8) return G4_OK;
   std::vector<MegaPhase> prog;
   size_t smem_f = 64;  // floats
-  auto wred_f = [&]() { return (size_t)kMegaWarps * 2 * NB * 32; };
-  auto note_full = [&](int K, int r_parts) { smem_f = std::max(smem_f, (size_t)(2 + r_parts) * NB * K + 32 * NB + wred_f()); };
+  auto wred_f = [&]() { return (size_t)2 * kMegaWarps * 2 * NB * 32; };  // double-buffered warp partials
+  auto note_full = [&](int K, int r_parts) { smem_f = std::max(smem_f, full_red(NB, K, r_parts) + 32 * NB + wred_f()); };
   auto note_slice = [&](const MegaPhase& ph) {
     const int sgk = ph.fmt == FMT_W4A16 ? 256 : 64;
-    smem_f = std::max(smem_f, (size_t)ph.upc * NB * ph.spu * sgk + wred_f());
+    smem_f = std::max(smem_f, (size_t)NB * ph.spu * sgk + wred_f());
   };
   // K-slice partial buffers for the branches summed by the next residual update
   float *o_parts = nullptr, *d_parts = nullptr, *pmp_parts = nullptr;
@@ -846,7 +842,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
     MegaPhase ph{};
     ph.type = PH_PMP;
     mega_lin(ph, h->pmp);
-    mega_plan(h->pmp, G, true, ph);
+    mega_plan(h->pmp, G, 8, ph);
     ph.in_mode = IN_EMBED;
     ph.x_stride = H;
     ph.y = pmp_parts;
@@ -879,7 +875,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
       MegaPhase ph{};
       ph.type = PH_GEMV;
       mega_lin(ph, Y.qkv);
-      mega_plan(Y.qkv, G, false, ph);
+      mega_plan(Y.qkv, G, 1, ph);
       ph.x_stride = H;
       ph.g_a = Y.in_norm;
       if (l == 0) {
@@ -941,19 +937,19 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
         return G4_OK;  // workspace sized for another plan: keep the launch-per-phase path
       size_t ab = 0;
       switch (Y.d) {
-        case 64: ab = attn_smem_bytes<64, 1>(1); break;
-        case 128: ab = attn_smem_bytes<128, 1>(1); break;
-        case 256: ab = attn_smem_bytes<256, 1>(1); break;
-        default: ab = attn_smem_bytes<512, 1>(1); break;
+        case 64: ab = attn_halves<64>() * attn_smem_bytes<64, 1>(1); break;
+        case 128: ab = attn_halves<128>() * attn_smem_bytes<128, 1>(1); break;
+        case 256: ab = attn_halves<256>() * attn_smem_bytes<256, 1>(1); break;
+        default: ab = attn_halves<512>() * attn_smem_bytes<512, 1>(1); break;
       }
-      smem_f = std::max(smem_f, (2 * ab + 3) / 4);
+      smem_f = std::max(smem_f, (ab + 3) / 4);
       prog.push_back(ph);
     }
     {  // O: K-slice partials summed by the gate/up residual update
       MegaPhase ph{};
       ph.type = PH_GEMV;
       mega_lin(ph, Y.o);
-      mega_plan(Y.o, G, true, ph);
+      mega_plan(Y.o, G, 4, ph);
       ph.in_mode = IN_PLAIN;
       ph.x_in = h->attn;
       ph.x_stride = nqd;
@@ -969,7 +965,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
       MegaPhase ph{};
       ph.type = PH_GEMV;
       mega_lin(ph, Y.gu);
-      mega_plan(Y.gu, G, false, ph);
+      mega_plan(Y.gu, G, 1, ph);
       ph.in_mode = IN_RESID;
       ph.x_in = cur;
       ph.x_stride = H;
@@ -992,7 +988,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
       MegaPhase ph{};
       ph.type = PH_GEMV;
       mega_lin(ph, Y.down);
-      mega_plan(Y.down, G, true, ph);
+      mega_plan(Y.down, G, 4, ph);
       ph.in_mode = IN_PLAIN;
       ph.x_in = h->act;
       ph.x_stride = Y.F;
@@ -1008,7 +1004,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
       MegaPhase ph{};
       ph.type = PH_GEMV;
       mega_lin(ph, Y.pg);
-      mega_plan(Y.pg, G, false, ph);
+      mega_plan(Y.pg, G, 1, ph);
       ph.in_mode = IN_RESID;
       ph.x_in = cur;
       ph.x_stride = H;
@@ -1033,7 +1029,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
       MegaPhase ph{};
       ph.type = PH_GEMV;
       mega_lin(ph, Y.pp);
-      mega_plan(Y.pp, G, false, ph);
+      mega_plan(Y.pp, G, 1, ph);
       ph.in_mode = IN_PLAIN;
       ph.x_in = h->pg;
       ph.x_stride = P;
@@ -1050,6 +1046,8 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
     MegaPhase ph{};
     ph.type = PH_LMHEAD;
     mega_lin(ph, h->lm);
+    mega_plan(h->lm, G, 1, ph);
+    ph.epi = EPI_ARGMAX;
     ph.in_mode = IN_RESID;
     ph.x_in = cur;
     ph.x_stride = H;
@@ -1093,7 +1091,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
     }
     prog[idx].trace_x = L - 1;                    // lm_head
   }
-  h->mega_smem = smem_f * 4 + 1024;
+  h->mega_smem = kRingBytes + smem_f * 4;
   int optin = init_kernel_attrs(h->device);
   if ((int)h->mega_smem > optin) return G4_OK;
   int nb1 = 0, nb2 = 0;
