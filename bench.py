@@ -104,6 +104,12 @@ def algorithmic_bytes(cfg, fmt, batch, positions):
     return wbytes, float(np.mean(kv))
 
 
+# DRAM traffic / algorithmic bytes of a kernel, from one ncu capture of its current code
+# (profiles/gemv_w4a16_e2b_v8k_b1_full.md); traffic scales with the rows a launch streams.
+# Keyed by (weight format, phase); a kernel changed since its capture has no entry.
+MEASURED_TRAFFIC_RATIO = {("w4a16", "gemv.gate_up"): 10715392 / 10616832}
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -351,7 +357,9 @@ def run_gpu(args, wl, cfg, fmt):
                    "seed": args.seed},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4),
-                     "traffic": None, "bytes_per_launch": dom_bytes, "ms_per_launch": round(dom_ms, 5),
+                     "traffic": (round(dom_bytes * MEASURED_TRAFFIC_RATIO[(fmt, dom_name)])
+                                 if (fmt, dom_name) in MEASURED_TRAFFIC_RATIO else None),
+                     "bytes_per_launch": dom_bytes, "ms_per_launch": round(dom_ms, 5),
                      "peak_source": peak_src},
         "step_roofline": {"bytes_per_step": step_bytes, "weight_bytes": wbytes, "kv_and_rows_bytes": kvbytes,
                           "achieved": round(step_bytes / (ms_max / K / 1e3) / 1e9, 1), "peak": peak,
