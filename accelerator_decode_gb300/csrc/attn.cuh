@@ -217,9 +217,22 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
     named_sync(bar_id, kAttnThreads);
     const __nv_bfloat16* Kt = Ks + (size_t)st * TD;
     const __nv_bfloat16* Vt = Vs + (size_t)st * TD;
-    // scores: warp per key, lanes over D
-    for (int jj = warp; jj < kAttnTile; jj += kAttnThreads / 32) {
+    // scores: warp per key, lanes over D.  A warp's keys (jj = warp + 4 q) are dotted first and
+    // reduced together, so the shuffle chains overlap; zero-filled rows past tn are skipped.
+    constexpr int KPW = kAttnTile / (kAttnThreads / 32);
+    float qreg[PL];
+    if constexpr (HPC == 1) {
+#pragma unroll
+      for (int e = 0; e < PL; ++e) qreg[e] = qs[lane * PL + e];
+    }
+    float dq[HPC][KPW];
+#pragma unroll
+    for (int q = 0; q < KPW; ++q) {
+      const int jj = warp + q * (kAttnThreads / 32);
       const int j = t0 + jj;
+#pragma unroll
+      for (int h = 0; h < HPC; ++h) dq[h][q] = 0.f;
+      if (jj >= tn) continue;
       float kv[PL];
       if (use_new && j == p) {
 #pragma unroll
@@ -243,10 +256,26 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
 #pragma unroll
       for (int h = 0; h < HPC; ++h) {
         float d = 0.f;
+        if constexpr (HPC == 1) {
 #pragma unroll
-        for (int e = 0; e < PL; ++e) d += qs[h * D + lane * PL + e] * kv[e];
-        d = warp_sum(d);
-        if (lane == 0) sc[h * kAttnTile + jj] = (jj < tn) ? d * a.scale : -INFINITY;
+          for (int e = 0; e < PL; ++e) d += qreg[e] * kv[e];
+        } else {
+#pragma unroll
+          for (int e = 0; e < PL; ++e) d += qs[h * D + lane * PL + e] * kv[e];
+        }
+        dq[h][q] = d;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < KPW; ++q)
+#pragma unroll
+      for (int h = 0; h < HPC; ++h) dq[h][q] = warp_sum(dq[h][q]);
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < KPW; ++q) {
+        const int jj = warp + q * (kAttnThreads / 32);
+#pragma unroll
+        for (int h = 0; h < HPC; ++h) sc[h * kAttnTile + jj] = (jj < tn) ? dq[h][q] * a.scale : -INFINITY;
       }
     }
     named_sync(bar_id, kAttnThreads);
@@ -274,6 +303,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
 #pragma unroll
         for (int e = 0; e < PT; ++e) acc[h][e] *= r;
       }
+#pragma unroll 4
       for (int jj = 0; jj < tn; ++jj) {
         const int j = t0 + jj;
         float vv[PT];
