@@ -45,7 +45,7 @@ struct GemmArgs {
   int logits_stride;
   float* am_val;         // [nb][gridDim.x]
   int* am_idx;
-  float* part;           // [ksplit][nb][n_mtiles * 128]
+  float* part;           // [ksplit][n_mtiles * 128 rows][64 columns]
   unsigned* counters;    // per M tile
   int n_mtiles;
   int* err;
@@ -314,10 +314,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     const int rows_total = a.n_mtiles * kTcM;
     bool final_ok = have;
     if (a.ksplit > 1) {
+      // partials [ksplit][row][64 columns]: each row's bpad columns are contiguous, so a thread
+      // moves them as bpad / 4 float4 (written and read back with all loads of a split in flight)
+      float4* prow = reinterpret_cast<float4*>(a.part) + ((size_t)ks * rows_total + row) * 16;
       if (have) {
 #pragma unroll
-        for (int b = 0; b < 64; ++b)
-          if (b < a.nb) a.part[((size_t)ks * a.nb + b) * rows_total + row] = v[b];
+        for (int c = 0; c < 16; ++c)
+          if (4 * c < a.bpad) prow[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
       }
       __threadfence();
       asm volatile("bar.sync 1, 128;\n" ::: "memory");
@@ -328,59 +331,83 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
         __threadfence();
 #pragma unroll
         for (int b = 0; b < 64; ++b) v[b] = 0.f;
-        for (int q = 0; q < a.ksplit; ++q) {  // split order: deterministic; 64 loads in flight
-          const float* pq = a.part + (size_t)q * a.nb * rows_total + row;
+        for (int q = 0; q < a.ksplit; ++q) {  // split order: deterministic
+          const float4* pq = reinterpret_cast<const float4*>(a.part) + ((size_t)q * rows_total + row) * 16;
+          float4 t[16];
 #pragma unroll
-          for (int b = 0; b < 64; ++b)
-            if (b < a.nb) v[b] += ldcg(pq + (size_t)b * rows_total);
+          for (int c = 0; c < 16; ++c) t[c] = (4 * c < a.bpad) ? __ldcg(pq + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            v[4 * c] += t[c].x;
+            v[4 * c + 1] += t[c].y;
+            v[4 * c + 2] += t[c].z;
+            v[4 * c + 3] += t[c].w;
+          }
         }
         if (m == 0) a.counters[mt] = 0u;
       }
     }
     if (final_ok) {
+      // the stage buffers are idle once the accumulator is complete: exchange space for the
+      // epilogues below (128 rows x 64 columns of fp32 at most, within one stage)
+      float* ex = reinterpret_cast<float*>(stage0);
       if (a.epi == EPI_GEGLU) {
-        // rows interleave 32-row blocks: gate j, up j, gate j+1, up j+1 (warps 0..3)
+        // rows interleave 32-row blocks: gate j, up j, gate j+1, up j+1 (warps 0..3); the up
+        // rows hand all their columns to the gate rows through shared memory at once
         const int pair = warp >> 1;
         const bool is_up = warp & 1;
         const int n = mt * 64 + pair * 32 + ln;
+        if (is_up) {
 #pragma unroll
-        for (int b = 0; b < 64; ++b) {
-          if (b >= a.nb) break;
-          if (is_up) xch[pair * 32 + ln] = v[b];
-          asm volatile("bar.sync 1, 128;\n" ::: "memory");
-          if (!is_up && n < a.n_valid) a.y[(size_t)b * a.y_stride + n] = gelu_tanh(v[b]) * xch[pair * 32 + ln];
-          asm volatile("bar.sync 1, 128;\n" ::: "memory");
+          for (int b = 0; b < 64; ++b)
+            if (b < a.nb) ex[(pair * 64 + b) * 32 + ln] = v[b];
+        }
+        asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        if (!is_up && n < a.n_valid) {
+#pragma unroll
+          for (int b = 0; b < 64; ++b)
+            if (b < a.nb) v[b] = gelu_tanh(v[b]) * ex[(pair * 64 + b) * 32 + ln];
+#pragma unroll
+          for (int b = 0; b < 64; ++b)
+            if (b < a.nb) a.y[(size_t)b * a.y_stride + n] = v[b];
         }
       } else if (a.epi == EPI_ARGMAX) {
-        // per column b: max over this tile's rows -> one partial per (b, CTA)
-        float* bv = xch;                                   // [4] per warp
-        int* bi = reinterpret_cast<int*>(xch + 4);
+        // logits out; then per column b the max over the tile's 128 rows, warp w taking columns
+        // w, w + 4, ...: one partial per (b, CTA)
+        if (a.logits && row < a.n_valid) {
 #pragma unroll
-        for (int b = 0; b < 64; ++b) {
-          if (b >= a.nb) break;
-          float x = v[b];
-          int idx = row;
-          if (row >= a.n_valid) { x = __int_as_float(0x7fc00000); idx = 0x7fffffff; }
-          else if (a.logits) a.logits[(size_t)b * a.logits_stride + row] = x;
-          warp_argmax(x, idx);
-          if (ln == 0) { bv[warp] = x; bi[warp] = idx; }
-          asm volatile("bar.sync 1, 128;\n" ::: "memory");
-          if (m == 0) {
-            for (int w = 1; w < 4; ++w)
-              if (argmax_better(bv[w], bi[w], bv[0], bi[0])) { bv[0] = bv[w]; bi[0] = bi[w]; }
-            a.am_val[(size_t)b * gridDim.x + blockIdx.x] = bv[0];
-            a.am_idx[(size_t)b * gridDim.x + blockIdx.x] = bi[0];
+          for (int b = 0; b < 64; ++b)
+            if (b < a.nb) a.logits[(size_t)b * a.logits_stride + row] = v[b];
+        }
+#pragma unroll
+        for (int b = 0; b < 64; ++b)
+          if (b < a.nb) ex[b * kTcM + m] = row < a.n_valid ? v[b] : __int_as_float(0x7fc00000);
+        asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        for (int b = warp; b < a.nb; b += 4) {
+          float x = __int_as_float(0x7fc00000);
+          int idx = 0x7fffffff;
+#pragma unroll
+          for (int j = 0; j < kTcM / 32; ++j) {
+            const int r = ln + 32 * j;
+            const float c = ex[b * kTcM + r];
+            const int ci = mt * kTcM + r;
+            if (ci < a.n_valid && argmax_better(c, ci, x, idx)) { x = c; idx = ci; }
           }
-          asm volatile("bar.sync 1, 128;\n" ::: "memory");
+          warp_argmax(x, idx);
+          if (ln == 0) {
+            a.am_val[(size_t)b * gridDim.x + blockIdx.x] = x;
+            a.am_idx[(size_t)b * gridDim.x + blockIdx.x] = idx;
+          }
         }
       } else if (row < a.n_valid) {
+        if (a.epi == EPI_PLE) {  // every multiplier is loaded before the first store
 #pragma unroll
-        for (int b = 0; b < 64; ++b) {
-          if (b >= a.nb) break;
-          float o = v[b];
-          if (a.epi == EPI_PLE) o = gelu_tanh(o) * a.ple[(size_t)b * a.ple_stride + row];
-          a.y[(size_t)b * a.y_stride + row] = o;
+          for (int b = 0; b < 64; ++b)
+            if (b < a.nb) v[b] = gelu_tanh(v[b]) * a.ple[(size_t)b * a.ple_stride + row];
         }
+#pragma unroll
+        for (int b = 0; b < 64; ++b)
+          if (b < a.nb) a.y[(size_t)b * a.y_stride + row] = v[b];
       }
     }
   }
