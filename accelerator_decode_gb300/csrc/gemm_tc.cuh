@@ -440,39 +440,51 @@ struct PrepArgs {
   uint8_t* xt;
 };
 
+// Shared memory of prep_x_kernel: x row and residual branch (fp32, kpad each), then both gain
+// vectors (bf16, kpad each).
+__host__ __device__ inline size_t prep_smem_bytes(int kpad) { return (size_t)kpad * (2 * 4 + 2 * 2); }
+
 __global__ void __launch_bounds__(256) prep_x_kernel(const PrepArgs a) {
-  extern __shared__ __align__(16) float prow[];  // [kpad]
+  extern __shared__ __align__(16) float prow[];  // [kpad] | residual [kpad] | g_r, g_a [kpad] bf16
   __shared__ float red[32];
-  pdl_trigger();
-  pdl_wait();
   const int b = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  float* rrow = prow + a.kpad;
+  __nv_bfloat16* gr_s = reinterpret_cast<__nv_bfloat16*>(rrow + a.kpad);
+  __nv_bfloat16* ga_s = gr_s + a.kpad;
+  const bool resid = a.pro == PRO_RESID, norm = a.pro != PRO_PLAIN && a.g_a != nullptr;
+  pdl_trigger();
+  // gains are weights: staged before waiting for the previous kernel
+  for (int c = tid; c < a.K / 8; c += nt) {
+    if (resid) cp_async16(gr_s + 8 * c, a.g_r + 8 * c, true);
+    if (norm) cp_async16(ga_s + 8 * c, a.g_a + 8 * c, true);
+  }
+  pdl_wait();
   const float* x = a.x_in + (size_t)b * a.x_stride;
-  float* rrow = prow + a.kpad;  // [K] residual branch (PRO_RESID)
   for (int c = tid; c < a.kpad / 4; c += nt) {
     const bool ok = 4 * c < a.K;
     cp_async16(prow + 4 * c, ok ? x + 4 * c : x, ok);
-    if (a.pro == PRO_RESID && ok) cp_async16(rrow + 4 * c, a.r_in + (size_t)b * a.r_stride + 4 * c, true);
+    if (resid && ok) cp_async16(rrow + 4 * c, a.r_in + (size_t)b * a.r_stride + 4 * c, true);
   }
   cp_async_wait_all();
   __syncthreads();
-  if (a.pro == PRO_RESID) {
+  // the loops below read only shared memory
+  if (resid) {
     const float* r = rrow;
     float ss[1] = {0.f};
     for (int k = tid; k < a.K; k += nt) ss[0] += r[k] * r[k];
     block_sum<1>(ss, red);
-    const float rd = rms_denom(ss[0], a.K, a.eps);
-    for (int k = tid; k < a.K; k += nt) {
-      prow[k] = (prow[k] + (r[k] / rd) * bf16f(a.g_r[k])) * a.lambda;
-      a.x_out[(size_t)b * a.x_stride + k] = prow[k];
-    }
+    const float rd = rms_denom(ss[0], a.K, a.eps), lambda = a.lambda;
+    for (int k = tid; k < a.K; k += nt) prow[k] = (prow[k] + (r[k] / rd) * bf16f(gr_s[k])) * lambda;
     __syncthreads();
+    float* xo = a.x_out + (size_t)b * a.x_stride;
+    for (int c = tid; c < a.K / 4; c += nt) reinterpret_cast<float4*>(xo)[c] = reinterpret_cast<const float4*>(prow)[c];
   }
-  if (a.pro != PRO_PLAIN && a.g_a != nullptr) {
+  if (norm) {
     float ss[1] = {0.f};
     for (int k = tid; k < a.K; k += nt) ss[0] += prow[k] * prow[k];
     block_sum<1>(ss, red);
     const float ad = rms_denom(ss[0], a.K, a.eps);
-    for (int k = tid; k < a.K; k += nt) prow[k] = (prow[k] / ad) * bf16f(a.g_a[k]);
+    for (int k = tid; k < a.K; k += nt) prow[k] = (prow[k] / ad) * bf16f(ga_s[k]);
     __syncthreads();
   }
   const size_t tile = (size_t)a.bpad * 128;
