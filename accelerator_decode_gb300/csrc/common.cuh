@@ -97,6 +97,11 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pr
   const int sz = pred ? 16 : 0;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(sz) : "memory");
 }
+// 4-byte global -> shared async copy (through L1; both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(s), "l"(gmem) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // Programmatic dependent launch.  Before pdl_wait() a kernel may only read data that no

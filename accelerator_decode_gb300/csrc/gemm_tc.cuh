@@ -331,17 +331,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
         __threadfence();
 #pragma unroll
         for (int b = 0; b < 64; ++b) v[b] = 0.f;
-        for (int q = 0; q < a.ksplit; ++q) {  // split order: deterministic
+        // Each thread streams its row of every split's partial into its own slots of a 4-deep
+        // shared ring with cp.async (up to 3 splits in flight), summing in split order.
+        const int nc = a.bpad / 4;
+        float4* qb = reinterpret_cast<float4*>(stage0);  // [4][nc][128 rows]
+        auto issue = [&](int q) {
           const float4* pq = reinterpret_cast<const float4*>(a.part) + ((size_t)q * rows_total + row) * 16;
-          float4 t[16];
-#pragma unroll
-          for (int c = 0; c < 16; ++c) t[c] = (4 * c < a.bpad) ? __ldcg(pq + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          float4* dst = qb + (size_t)(q & 3) * nc * kTcM;
+          for (int c = 0; c < nc; ++c) cp_async16(dst + c * kTcM + m, pq + c, true);
+          asm volatile("cp.async.commit_group;\n" ::: "memory");
+        };
+        for (int q = 0; q < 3 && q < a.ksplit; ++q) issue(q);
+        for (int q = 0; q < a.ksplit; ++q) {
+          if (q + 3 < a.ksplit) issue(q + 3);
+          const int pending = min(a.ksplit, q + 4) - (q + 1);  // groups allowed to stay in flight
+          if (pending >= 3) asm volatile("cp.async.wait_group 3;\n" ::: "memory");
+          else if (pending == 2) asm volatile("cp.async.wait_group 2;\n" ::: "memory");
+          else if (pending == 1) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+          else asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+          const float4* src = qb + (size_t)(q & 3) * nc * kTcM;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            v[4 * c] += t[c].x;
-            v[4 * c + 1] += t[c].y;
-            v[4 * c + 2] += t[c].z;
-            v[4 * c + 3] += t[c].w;
+            if (c < nc) {
+              const float4 t = src[c * kTcM + m];
+              v[4 * c] += t.x;
+              v[4 * c + 1] += t.y;
+              v[4 * c + 2] += t.z;
+              v[4 * c + 3] += t.w;
+            }
           }
         }
         if (m == 0) a.counters[mt] = 0u;
@@ -349,8 +366,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     }
     if (final_ok) {
       // the stage buffers are idle once the accumulator is complete: exchange space for the
-      // epilogues below (128 rows x 64 columns of fp32 at most, within one stage)
-      float* ex = reinterpret_cast<float*>(stage0);
+      // epilogues below (128 rows x bpad columns of fp32)
+      // past the split-K ring (4 x 128 x bpad fp32), which other threads may still be reading
+      float* ex = reinterpret_cast<float*>(stage0 + (size_t)4 * kTcM * a.bpad * 4);
       if (a.epi == EPI_GEGLU) {
         // rows interleave 32-row blocks: gate j, up j, gate j+1, up j+1 (warps 0..3); the up
         // rows hand all their columns to the gate rows through shared memory at once
@@ -400,10 +418,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
           }
         }
       } else if (row < a.n_valid) {
-        if (a.epi == EPI_PLE) {  // every multiplier is loaded before the first store
+        if (a.epi == EPI_PLE) {
+          // the row's multipliers arrive by cp.async (one round trip, nothing waits on a
+          // single load), [b][128 rows] so the accesses are conflict-free
+          float* pl = ex;
 #pragma unroll
           for (int b = 0; b < 64; ++b)
-            if (b < a.nb) v[b] = gelu_tanh(v[b]) * a.ple[(size_t)b * a.ple_stride + row];
+            if (b < a.nb) cp_async4(pl + b * kTcM + m, a.ple + (size_t)b * a.ple_stride + row);
+          cp_async_wait_all();
+#pragma unroll
+          for (int b = 0; b < 64; ++b)
+            if (b < a.nb) v[b] = gelu_tanh(v[b]) * pl[b * kTcM + m];
         }
 #pragma unroll
         for (int b = 0; b < 64; ++b)
