@@ -169,10 +169,11 @@ int sgk(int fmt) { return fmt == G4_W4A16 ? Fmt<FMT_W4A16>::SGK : Fmt<FMT_BF16>:
 // for very tall matrices.
 void plan_lin(Lin& L, int sms, bool whole_k) {
   const int n_rg = L.n_rb / L.R;
-  int spw = 1;
-  auto sgpc = [&](int s) { return std::min(L.S, kGemvWarps * s); };
-  while (sgpc(spw) < L.S && (whole_k || (long)n_rg * cdiv(L.S, sgpc(spw)) > 3L * sms)) spw *= 2;
-  L.sg_per_cta = sgpc(spw);
+  // start near one supergroup per warp, halve the split while the grid exceeds 3 waves; the
+  // K slices are balanced (warps share a slice's tiles, whatever its supergroup count)
+  int ks = whole_k ? 1 : cdiv(L.S, kGemvWarps);
+  while (ks > 1 && (long)n_rg * ks > 3L * sms) ks = cdiv(ks, 2);
+  L.sg_per_cta = cdiv(L.S, ks);
   L.ksplit = cdiv(L.S, L.sg_per_cta);
 }
 

@@ -254,23 +254,36 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
   const int k1 = min(a.K, sg1 * F::SGK);
   const GemvSmem L = gemv_smem_plan(NB, R, kc, a.pro, a.norm_n, a.ksplit);
   const int rows_total = a.n_rb * 32;
-  const int sg_first = sg0 + warp;
+  // Warp w takes tiles i = w, w + 4, ... of the CTA's K slice (tile i: supergroup sg0 + i / 8,
+  // tile i % 8), so every warp has work whatever the slice's supergroup count.  Weights move
+  // through a two-group register pipeline of kGrp tiles; the first group is loaded before
+  // waiting on the previous kernel, the next row group's first group before the reduction.
+  constexpr int kGrp = 8 / R;  // 8 tiles (R = 1) or 4 tile pairs (R = 2) per group
+  const int nT = (sg1 - sg0) * 8;
+  const int nj = nT > warp ? (nT - warp + kGemvWarps - 1) / kGemvWarps : 0;  // tiles of this warp
+  const int ng = (nj + kGrp - 1) / kGrp;
 
   pdl_trigger();
-  uint4 wbuf[R][8];
-  uint4 sbuf[R];
-  auto load_sg = [&](int rg_, int s) {
+  uint4 wb0[kGrp][R], wb1[kGrp][R];
+  uint32_t sw0[kGrp][R], sw1[kGrp][R];
+  auto load_grp = [&](uint4 (&wb)[kGrp][R], uint32_t (&sw)[kGrp][R], int rg_, int gi) {
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int rb = rg_ * R + r;
-      const uint4* base = a.qw + ((size_t)rb * a.tiles + (size_t)s * 8) * 32 + lane;
+    for (int g = 0; g < kGrp; ++g) {
+      const int i = warp + kGemvWarps * (gi * kGrp + g);
+      if (i < nT) {
+        const int s = sg0 + (i >> 3), t = i & 7;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) wbuf[r][t] = __ldg(base + t * 32);
-      if constexpr (FMT == FMT_W4A16) sbuf[r] = __ldg(a.sc + ((size_t)rb * a.S + s) * 32 + lane);
+        for (int r = 0; r < R; ++r) {
+          const int rb = rg_ * R + r;
+          wb[g][r] = __ldg(a.qw + ((size_t)rb * a.tiles + (size_t)s * 8 + t) * 32 + lane);
+          if constexpr (FMT == FMT_W4A16)
+            sw[g][r] = __ldg(reinterpret_cast<const uint32_t*>(a.sc + ((size_t)rb * a.S + s) * 32 + lane) + (t >> 1));
+        }
+      }
     }
   };
   int rg = blockIdx.x / a.ksplit;
-  if (rg < n_rg && sg_first < sg1) load_sg(rg, sg_first);  // weights never depend on activations
+  if (rg < n_rg && ng > 0) load_grp(wb0, sw0, rg, 0);  // weights never depend on activations
   pdl_wait();
   gemv_prologue<NB>(a, smem, L, kc, k0, k1);
 
@@ -289,26 +302,35 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
-    int sg = sg_first;
-    while (sg < sg1) {
-      const float* xsg = xs + (sg - sg0) * F::SGK;
+    auto compute_grp = [&](const uint4 (&wb)[kGrp][R], const uint32_t (&sw)[kGrp][R], int gi) {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
+      for (int g = 0; g < kGrp; ++g) {
+        const int i = warp + kGemvWarps * (gi * kGrp + g);
+        if (i < nT) {
+          const int t = i & 7;
+          const float* xt = xs + (i >> 3) * F::SGK + t * F::TK;
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          uint32_t s2 = 0;
-          if constexpr (FMT == FMT_W4A16) {
-            const uint32_t sw = (&sbuf[r].x)[t >> 1];
-            const uint32_t hh = (t & 1) ? (sw >> 16) : (sw & 0xFFFFu);
-            s2 = hh | (hh << 16);
+          for (int r = 0; r < R; ++r) {
+            uint32_t s2 = 0;
+            if constexpr (FMT == FMT_W4A16) {
+              const uint32_t hh = (t & 1) ? (sw[g][r] >> 16) : (sw[g][r] & 0xFFFFu);
+              s2 = hh | (hh << 16);
+            }
+            tile_fma<FMT, NB>(wb[g][r], s2, xt, kc, acc[r]);
           }
-          tile_fma<FMT, NB>(wbuf[r][t], s2, xsg + t * F::TK, kc, acc[r]);
         }
       }
-      sg += kGemvWarps;
-      if (sg < sg1) load_sg(rg, sg);
-      else if (rg + rg_step < n_rg && sg_first < sg1) load_sg(rg + rg_step, sg_first);  // next row group
+    };
+    for (int gi = 0; gi < ng; ++gi) {
+      if ((gi & 1) == 0) {
+        if (gi + 1 < ng) load_grp(wb1, sw1, rg, gi + 1);
+        compute_grp(wb0, sw0, gi);
+      } else {
+        if (gi + 1 < ng) load_grp(wb0, sw0, rg, gi + 1);
+        compute_grp(wb1, sw1, gi);
+      }
     }
+    if (rg + rg_step < n_rg && ng > 0) load_grp(wb0, sw0, rg + rg_step, 0);  // next row group
 
     // cross-warp reduction in fixed warp order
 #pragma unroll
