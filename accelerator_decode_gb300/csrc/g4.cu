@@ -169,9 +169,9 @@ int sgk(int fmt) { return fmt == G4_W4A16 ? Fmt<FMT_W4A16>::SGK : Fmt<FMT_BF16>:
 // for very tall matrices.
 void plan_lin(Lin& L, int sms, bool whole_k) {
   const int n_rg = L.n_rb / L.R;
-  // start near one supergroup per warp, halve the split while the grid exceeds 3 waves; the
+  // start at one supergroup per CTA, halve the split while the grid exceeds 3 CTAs per SM; the
   // K slices are balanced (warps share a slice's tiles, whatever its supergroup count)
-  int ks = whole_k ? 1 : cdiv(L.S, kGemvWarps);
+  int ks = whole_k ? 1 : L.S;
   while (ks > 1 && (long)n_rg * ks > 3L * sms) ks = cdiv(ks, 2);
   L.sg_per_cta = cdiv(L.S, ks);
   L.ksplit = cdiv(L.S, L.sg_per_cta);
