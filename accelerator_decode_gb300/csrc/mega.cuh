@@ -30,6 +30,7 @@ namespace g4 {
 
 constexpr int kMegaThreads = 256;
 constexpr int kMegaWarps = kMegaThreads / 32;
+static_assert(kMegaWarps == 8, "projection items give warp w tile w of each supergroup");
 constexpr unsigned long long kBarrierTimeoutNs = 2000000000ull;  // 2 s
 constexpr int kPhaseBufs = 4;  // phase descriptors p .. p + 3 staged in shared memory
 
@@ -381,27 +382,24 @@ __device__ void ring_fill(const MegaArgs& a, MegaRing& R, unsigned char* ring, c
   }
 }
 
-// Bounded wait for item `seq` (all threads).  Returns false for every thread of the CTA when
-// any of them gave up (the CTA then leaves the phase program).
-__device__ bool ring_wait(const MegaArgs& a, MegaRing& R, uint32_t seq) {
+// Bounded wait for item `seq` by each warp on its own (no CTA barrier).  On expiry the warp
+// sets the timeout bit, the abort flag and R.dead; the caller reads R.dead after its next
+// __syncthreads, so every thread of the CTA leaves together.
+__device__ void ring_wait(const MegaArgs& a, MegaRing& R, uint32_t seq) {
   const int slot = seq % kRingSlots;
   const uint32_t parity = (seq / kRingSlots) & 1u;
-  bool ok = mbar_try(&R.full[slot], parity);
-  if (!ok) {
-    const unsigned long long t0 = globaltimer_ns();
-    volatile unsigned* abort_g = a.barrier + 1;
-    for (uint32_t it = 1; !ok; ++it) {
-      ok = mbar_try(&R.full[slot], parity);
-      if (!ok && (it & 1023u) == 0) {
-        if (*abort_g || globaltimer_ns() - t0 > kBarrierTimeoutNs) break;
-      }
-    }
-    if (!ok) {
-      set_err(a.err, G4_DEV_TIMEOUT);
-      *abort_g = 1u;
-    }
+  if (mbar_try(&R.full[slot], parity)) return;
+  const unsigned long long t0 = globaltimer_ns();
+  volatile unsigned* abort_g = a.barrier + 1;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(&R.full[slot], parity)) return;
+    if ((it & 1023u) == 0 && (*abort_g || globaltimer_ns() - t0 > kBarrierTimeoutNs)) break;
   }
-  return __syncthreads_and(ok ? 1 : 0) != 0;
+  if ((threadIdx.x & 31) == 0) {
+    set_err(a.err, G4_DEV_TIMEOUT);
+    *abort_g = 1u;
+    R.dead = 1;
+  }
 }
 
 // Leaving the launch (normally or on abort): wait, bounded, for every issued, unconsumed item so
@@ -482,28 +480,43 @@ __device__ __noinline__ bool mega_proj(const MegaArgs& a, const MegaPhase& ph, f
 #pragma unroll
       for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
     for (int c = 0; c < g.n_chunks; ++c) {
-      if (!ring_wait(a, R, seq)) return false;
+      ring_wait(a, R, seq);
+      const bool live = !*reinterpret_cast<volatile int*>(&R.dead);
       const unsigned char* item = ring + R.off[seq % kRingSlots];
       const int c0 = c * ph.chunk_sg;
       const int csz = min(ph.chunk_sg, g.nsg - c0);
       const unsigned char* scb = item + (size_t)nR * csz * sgb;
-      for (int i = warp; i < csz * nR; i += kMegaWarps) {
-        const int sl = i / nR, r = i - sl * nR;
-        const uint4* wt = reinterpret_cast<const uint4*>(item + (size_t)(r * csz + sl) * sgb) + lane;
-        uint4 sv = make_uint4(0, 0, 0, 0);
-        if constexpr (FMT == FMT_W4A16) sv = reinterpret_cast<const uint4*>(scb + (size_t)(r * csz + sl) * kTileBytes)[lane];
-        const float* xsg = xs + (c0 + sl) * SGK;
+      // warp w takes tile t = w of every (supergroup, row block) pair of the item: eight warps,
+      // eight tiles per pair, so the item's tiles spread evenly over the CTA
+      {
+        const int t = warp;
+        const float* xt = xs + c0 * SGK + t * TK;
+        const int np = live ? csz * nR : 0;
+        for (int i0 = 0; i0 < np; i0 += 4) {
+          // four pairs' tiles and scales first, so their shared-memory loads overlap
+          uint4 wv[4];
+          uint32_t s2[4];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          uint32_t s2 = 0;
-          if constexpr (FMT == FMT_W4A16) {
-            const uint32_t sw = (&sv.x)[t >> 1];
-            const uint32_t hh = (t & 1) ? (sw >> 16) : (sw & 0xFFFFu);
-            s2 = hh | (hh << 16);
+          for (int u = 0; u < 4; ++u) {
+            const int i = min(i0 + u, np - 1);
+            const int sl = i / nR, r = i - sl * nR;
+            wv[u] = reinterpret_cast<const uint4*>(item + (size_t)(r * csz + sl) * sgb + t * kTileBytes)[lane];
+            s2[u] = 0;
+            if constexpr (FMT == FMT_W4A16) {
+              const uint32_t sw = reinterpret_cast<const uint32_t*>(scb + (size_t)(r * csz + sl) * kTileBytes + lane * 16)[t >> 1];
+              const uint32_t hh = (t & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+              s2[u] = hh | (hh << 16);
+            }
           }
-          const uint4 wv = wt[t * 32];
-          if (r == 0) tile_fma<FMT, NB>(wv, s2, xsg + t * TK, xs_stride, acc[0]);
-          else tile_fma<FMT, NB>(wv, s2, xsg + t * TK, xs_stride, acc[1]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u;
+            if (i < np) {
+              const int sl = i / nR, r = i - sl * nR;
+              if (r == 0) tile_fma<FMT, NB>(wv[u], s2[u], xt + sl * SGK, xs_stride, acc[0]);
+              else tile_fma<FMT, NB>(wv[u], s2[u], xt + sl * SGK, xs_stride, acc[1]);
+            }
+          }
         }
       }
       float* wr = wred + (size_t)(j & 1) * kMegaWarps * 2 * NB * 32;
@@ -514,6 +527,7 @@ __device__ __noinline__ bool mega_proj(const MegaArgs& a, const MegaPhase& ph, f
           for (int b = 0; b < NB; ++b) wr[warp * (2 * NB * 32) + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
       }
       __syncthreads();  // item consumed (and, on the last chunk, warp partials written)
+      if (R.dead) return false;  // a wait ran out (read after the barrier: uniform)
       ++seq;
       if (threadIdx.x == 0) {
         R.consumed = seq;
