@@ -524,11 +524,13 @@ void launch_attn_d(const AttnArgs& a, int hpc, int nb, cudaStream_t st) {
   }
 }
 
+// Query heads per attention unit.  One: a unit per (split, head, sequence) keeps every unit's
+// dependency chain short; at batch 64 this measured faster than eight heads per unit (which
+// share one K/V tile load but serialise eight heads' scores and outputs in one CTA).
 int attn_hpc(int nq, int nb) {
-  if (nb <= 2) return 1;
-  int h = 8;
-  while (h > 1 && nq % h) h >>= 1;
-  return h;
+  (void)nq;
+  (void)nb;
+  return 1;
 }
 int attn_nsplit(int sms, int nq, int hpc, int nb, int max_keys) {
   const int n_hg = nq / hpc;
