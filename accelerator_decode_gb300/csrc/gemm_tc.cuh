@@ -364,43 +364,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
         if (m == 0) a.counters[mt] = 0u;
       }
     }
+    // Epilogue.  The tile's columns go to shared memory once ([b][128 rows], past the split-K
+    // ring, which other threads may still be reading), and the variants below run as rolled
+    // loops over b: fully unrolled 64-column epilogues ran once per CTA from a cold
+    // instruction cache.  The stage buffers are idle once the accumulator is complete.
+    float* ex = reinterpret_cast<float*>(stage0 + (size_t)4 * kTcM * a.bpad * 4);  // [bpad][128]
+    float* pl = ex + (size_t)a.bpad * kTcM;                                        // [bpad][128]
     if (final_ok) {
-      // the stage buffers are idle once the accumulator is complete: exchange space for the
-      // epilogues below (128 rows x bpad columns of fp32)
-      // past the split-K ring (4 x 128 x bpad fp32), which other threads may still be reading
-      float* ex = reinterpret_cast<float*>(stage0 + (size_t)4 * kTcM * a.bpad * 4);
+#pragma unroll
+      for (int b = 0; b < 64; ++b)
+        if (b < a.bpad) ex[b * kTcM + m] = v[b];
+    }
+    asm volatile("bar.sync 1, 128;\n" ::: "memory");  // every CTA of the split reaches it
+    if (final_ok) {
       if (a.epi == EPI_GEGLU) {
-        // rows interleave 32-row blocks: gate j, up j, gate j+1, up j+1 (warps 0..3); the up
-        // rows hand all their columns to the gate rows through shared memory at once
-        const int pair = warp >> 1;
-        const bool is_up = warp & 1;
-        const int n = mt * 64 + pair * 32 + ln;
-        if (is_up) {
-#pragma unroll
-          for (int b = 0; b < 64; ++b)
-            if (b < a.nb) ex[(pair * 64 + b) * 32 + ln] = v[b];
-        }
-        asm volatile("bar.sync 1, 128;\n" ::: "memory");
-        if (!is_up && n < a.n_valid) {
-#pragma unroll
-          for (int b = 0; b < 64; ++b)
-            if (b < a.nb) v[b] = gelu_tanh(v[b]) * ex[(pair * 64 + b) * 32 + ln];
-#pragma unroll
-          for (int b = 0; b < 64; ++b)
-            if (b < a.nb) a.y[(size_t)b * a.y_stride + n] = v[b];
+        // rows interleave 32-row blocks: gate j, up j, gate j+1, up j+1 (warps 0..3)
+        if ((warp & 1) == 0) {
+          const int n = mt * 64 + (warp >> 1) * 32 + ln;
+          if (n < a.n_valid)
+            for (int b = 0; b < a.nb; ++b)
+              a.y[(size_t)b * a.y_stride + n] = gelu_tanh(ex[b * kTcM + m]) * ex[b * kTcM + m + 32];
         }
       } else if (a.epi == EPI_ARGMAX) {
         // logits out; then per column b the max over the tile's 128 rows, warp w taking columns
         // w, w + 4, ...: one partial per (b, CTA)
-        if (a.logits && row < a.n_valid) {
-#pragma unroll
-          for (int b = 0; b < 64; ++b)
-            if (b < a.nb) a.logits[(size_t)b * a.logits_stride + row] = v[b];
-        }
-#pragma unroll
-        for (int b = 0; b < 64; ++b)
-          if (b < a.nb) ex[b * kTcM + m] = row < a.n_valid ? v[b] : __int_as_float(0x7fc00000);
-        asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        if (a.logits && row < a.n_valid)
+          for (int b = 0; b < a.nb; ++b) a.logits[(size_t)b * a.logits_stride + row] = ex[b * kTcM + m];
         for (int b = warp; b < a.nb; b += 4) {
           float x = __int_as_float(0x7fc00000);
           int idx = 0x7fffffff;
@@ -421,18 +410,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
         if (a.epi == EPI_PLE) {
           // the row's multipliers arrive by cp.async (one round trip, nothing waits on a
           // single load), [b][128 rows] so the accesses are conflict-free
-          float* pl = ex;
-#pragma unroll
-          for (int b = 0; b < 64; ++b)
-            if (b < a.nb) cp_async4(pl + b * kTcM + m, a.ple + (size_t)b * a.ple_stride + row);
+          for (int b = 0; b < a.nb; ++b) cp_async4(pl + b * kTcM + m, a.ple + (size_t)b * a.ple_stride + row);
           cp_async_wait_all();
-#pragma unroll
-          for (int b = 0; b < 64; ++b)
-            if (b < a.nb) v[b] = gelu_tanh(v[b]) * pl[b * kTcM + m];
+          for (int b = 0; b < a.nb; ++b)
+            a.y[(size_t)b * a.y_stride + row] = gelu_tanh(ex[b * kTcM + m]) * pl[b * kTcM + m];
+        } else {
+          for (int b = 0; b < a.nb; ++b) a.y[(size_t)b * a.y_stride + row] = ex[b * kTcM + m];
         }
-#pragma unroll
-        for (int b = 0; b < 64; ++b)
-          if (b < a.nb) a.y[(size_t)b * a.y_stride + row] = v[b];
       }
     }
   }
