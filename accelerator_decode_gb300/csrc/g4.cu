@@ -380,7 +380,8 @@ int tc_nkb(const Lin& L) { return cdiv(L.K, kTcKB); }
 void tc_plan(const Lin& L, int sms, bool whole_k, int* ksplit, int* kbps) {
   const int nmt = L.n_rb / 4, nkb = tc_nkb(L);
   // at least 4 k-blocks per split: the split-K reduction is not free
-  int k = whole_k ? 1 : std::max(1, std::min(cdiv(nkb, 4), sms / std::max(1, nmt)));
+  // and at most 6 splits: the last CTA's merge costs a few L2 round trips per 3 splits
+  int k = whole_k ? 1 : std::max(1, std::min({cdiv(nkb, 4), sms / std::max(1, nmt), 6}));
   *kbps = cdiv(nkb, k);
   *ksplit = cdiv(nkb, *kbps);
 }

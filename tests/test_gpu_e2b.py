@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from test_gpu_decode import GAP_TIE, LOGIT_TOL, _cos, gpu_generate
+from test_gpu_decode import COS_MIN, GAP_TIE, LOGIT_TOL, _cos, gpu_generate
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -64,3 +64,27 @@ def test_long_context_e2b_heads(rt, batch):
     assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL
     ok = ref["gaps"].T > GAP_TIE
     assert np.all((toks == ref["tokens"]) | ~ok)
+
+
+def test_e2b_batch64_sampled_sequences(rt):
+    """The batch-64 workload's launch configuration (tensor-core GEMMs, 64 sequences per step)
+    at E2B size.  Sequences are independent, so the oracle decodes a sample of them alone;
+    every sampled sequence's logits must match, teacher-forced on the oracle's tokens."""
+    cfg = synth.get_config("e2b")
+    w = synth.make_weights(cfg, "w4a16", seed=0, qk_gain=QK_GAIN)
+    B, T, n_out = 64, 8, 3
+    prompts = synth.make_prompts(cfg["vocab"], B, T, seed=3)
+    sample = [0, 17, 42, 63]
+    ref = oracle.Oracle(cfg, w, max_batch=len(sample), max_context=32).generate(prompts[sample], n_out,
+                                                                                keep_logits=True)
+    teacher = np.zeros((B, n_out), np.int32)
+    teacher[sample] = ref["tokens"]
+    dec = rt.Decoder(cfg, w, max_batch=B, max_context=32)
+    toks, logits = gpu_generate(dec, list(prompts), n_out, teacher=teacher)
+    assert dec.device_error()[1] == 0
+    dec.close()
+    got = logits[:, sample]
+    assert np.max(np.abs(got - ref["logits"])) <= LOGIT_TOL
+    assert min(_cos(got[s][i], ref["logits"][s][i]) for s in range(n_out) for i in range(len(sample))) >= COS_MIN
+    ok = ref["gaps"].T > GAP_TIE
+    assert np.all((toks[sample] == ref["tokens"]) | ~ok)
