@@ -666,7 +666,10 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       const int hpc = attn_hpc(c.num_q_heads, n);
       const int max_keys = Y.full ? c.max_context : std::min(c.sliding_window, c.max_context);
       a.nsplit = attn_nsplit(h->sms, c.num_q_heads, hpc, n, max_keys);
-      a.nstage = cdiv(max_keys, a.nsplit) > kAttnTile ? 2 : 1;
+      // double-buffered K/V tiles only while the grid fits on the SMs at one unit each: a
+      // larger grid needs the occupancy more than the overlap (the 512-wide tiles take 128 KB)
+      const long units = (long)n * (c.num_q_heads / hpc) * a.nsplit;
+      a.nstage = (cdiv(max_keys, a.nsplit) > kAttnTile && units <= h->sms) ? 2 : 1;
       a.ws_ml = h->attn_ml;
       a.ws_o = h->attn_o;
       a.counters = h->attn_cnt;
