@@ -403,7 +403,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
       float o[PT];
 #pragma unroll
       for (int e = 0; e < PT; ++e) o[e] = 0.f;
-#pragma unroll 4
+#pragma unroll 16
       for (int s = 0; s < a.nsplit; ++s) {
         const float w = wgt[s];
 #pragma unroll
