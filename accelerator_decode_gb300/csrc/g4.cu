@@ -311,9 +311,6 @@ void attrs_gemv(int optin) {
 template <int D>
 void attrs_attn(int optin) {
   set_max_dyn(attn_kernel<D, 1>, optin);
-  set_max_dyn(attn_kernel<D, 2>, optin);
-  set_max_dyn(attn_kernel<D, 4>, optin);
-  set_max_dyn(attn_kernel<D, 8>, optin);
 }
 std::mutex g_attr_mu;
 std::map<int, int> g_optin;  // device -> opt-in shared memory bytes
@@ -517,12 +514,8 @@ void launch_attn(const AttnArgs& a, int nb, cudaStream_t st) {
 }
 template <int D>
 void launch_attn_d(const AttnArgs& a, int hpc, int nb, cudaStream_t st) {
-  switch (hpc) {
-    case 1: launch_attn<D, 1>(a, nb, st); break;
-    case 2: launch_attn<D, 2>(a, nb, st); break;
-    case 4: launch_attn<D, 4>(a, nb, st); break;
-    default: launch_attn<D, 8>(a, nb, st); break;
-  }
+  (void)hpc;  // attn_hpc: one head per unit
+  launch_attn<D, 1>(a, nb, st);
 }
 
 // Query heads per attention unit.  One: a unit per (split, head, sequence) keeps every unit's

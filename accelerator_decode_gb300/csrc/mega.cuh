@@ -640,9 +640,9 @@ __device__ __noinline__ void mega_attn_d(const MegaArgs& a, const MegaPhase& ph,
   constexpr int H = attn_halves<D>();
   const int half = threadIdx.x >> 7;
   if (half >= H) return;
-  const int n_hg = ph.attn.nq / ph.attn_hpc;
-  const int units = ph.attn_units, nsplit = ph.attn.nsplit, hpc = ph.attn_hpc;
-  unsigned char* my = smem + half * (hpc == 1 ? attn_smem_bytes<D, 1>(ph.attn.nstage) : attn_smem_bytes<D, 8>(ph.attn.nstage));
+  const int n_hg = ph.attn.nq;  // one query head per unit
+  const int units = ph.attn_units, nsplit = ph.attn.nsplit;
+  unsigned char* my = smem + half * attn_smem_bytes<D, 1>(ph.attn.nstage);
   for (int u0 = blockIdx.x * H; u0 < units; u0 += gridDim.x * H) {
     const int u = u0 + half;
     const int b = u / (nsplit * n_hg);
@@ -652,8 +652,7 @@ __device__ __noinline__ void mega_attn_d(const MegaArgs& a, const MegaPhase& ph,
       aa.positions = a.positions;
       const int split = u % nsplit;
       const int hg = (u / nsplit) % n_hg;
-      if (hpc == 1) attn_unit<D, 1>(aa, split, hg, b, my, half * 128, 1 + half);
-      else attn_unit<D, 8>(aa, split, hg, b, my, half * 128, 1 + half);
+      attn_unit<D, 1>(aa, split, hg, b, my, half * 128, 1 + half);
     }
   }
 }
