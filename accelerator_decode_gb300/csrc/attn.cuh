@@ -58,6 +58,48 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// New K/V row of an owning layer at position p, on one warp: k = RoPE(RMSNorm(k) g_k), v,
+// both rounded to bf16.  Stores the row in the cache when `store`; copies the rounded values
+// to knew / vnew (shared, [D]) when they are given.  cs / sn: this lane's RoPE factors at p.
+template <int D>
+__device__ __forceinline__ void kv_row(const AttnArgs& a, const float* qraw, int slot, int p, const float (&cs)[D / 64],
+                                       const float (&sn)[D / 64], float* knew, float* vnew, bool store) {
+  const int lane = threadIdx.x & 31;
+  const float* kr = qraw + (size_t)a.nq * D;
+  const float* vr = kr + D;
+  float kv_[D / 32], vv_[D / 32], gk[D / 32];
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) {
+    kv_[e] = __ldcg(kr + lane + 32 * e);
+    vv_[e] = __ldcg(vr + lane + 32 * e);
+    gk[e] = bf16f(a.g_k[lane + 32 * e]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) ss += kv_[e] * kv_[e];
+  ss = warp_sum(ss);
+  const float den = rms_denom(ss, D, a.eps);
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) kv_[e] = (kv_[e] / den) * gk[e];
+  __nv_bfloat16* kdst = a.kc + ((size_t)slot * a.t_max + p) * D;
+  __nv_bfloat16* vdst = a.vc + ((size_t)slot * a.t_max + p) * D;
+#pragma unroll
+  for (int e = 0; e < D / 64; ++e) {
+    const int i = lane + 32 * e;
+    const float ka = kv_[e], kb = kv_[e + D / 64];
+    const __nv_bfloat16 k1 = __float2bfloat16_rn(ka * cs[e] - kb * sn[e]);
+    const __nv_bfloat16 k2 = __float2bfloat16_rn(kb * cs[e] + ka * sn[e]);
+    if (knew) { knew[i] = bf16f(k1); knew[i + D / 2] = bf16f(k2); }
+    if (store) { kdst[i] = k1; kdst[i + D / 2] = k2; }
+  }
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) {
+    const __nv_bfloat16 v1 = __float2bfloat16_rn(vv_[e]);
+    if (vnew) vnew[lane + 32 * e] = bf16f(v1);
+    if (store) vdst[lane + 32 * e] = v1;
+  }
+}
+
 // One (split, head group, sequence) unit on kAttnThreads threads; `asmem` holds
 // attn_smem_bytes<D, HPC>(a.nstage) bytes.  Called by attn_kernel and by the persistent step.
 template <int D, int HPC>
@@ -161,42 +203,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
     }
   }
   // ---- new K/V row of an owning layer (position p), computed by every CTA holding key p
-  if (use_new && warp == kKvWarp) {
-    const float* kr = qraw + (size_t)a.nq * D;
-    const float* vr = kr + D;
-    float kv_[D / 32], vv_[D / 32], gk[D / 32];
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      kv_[e] = __ldcg(kr + lane + 32 * e);
-      vv_[e] = __ldcg(vr + lane + 32 * e);
-      gk[e] = bf16f(a.g_k[lane + 32 * e]);
-    }
-    float ss = 0.f;
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) ss += kv_[e] * kv_[e];
-    ss = warp_sum(ss);
-    const float den = rms_denom(ss, D, a.eps);
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) kv_[e] = (kv_[e] / den) * gk[e];
-    __nv_bfloat16* kdst = a.kc + ((size_t)slot * a.t_max + p) * D;
-    __nv_bfloat16* vdst = a.vc + ((size_t)slot * a.t_max + p) * D;
-#pragma unroll
-    for (int e = 0; e < D / 64; ++e) {
-      const int i = lane + 32 * e;
-      const float ka = kv_[e], kb = kv_[e + D / 64];
-      const __nv_bfloat16 k1 = __float2bfloat16_rn(ka * cs[e] - kb * sn[e]);
-      const __nv_bfloat16 k2 = __float2bfloat16_rn(kb * cs[e] + ka * sn[e]);
-      knew[i] = bf16f(k1);
-      knew[i + D / 2] = bf16f(k2);
-      if (hg == 0) { kdst[i] = k1; kdst[i + D / 2] = k2; }
-    }
-#pragma unroll
-    for (int e = 0; e < D / 32; ++e) {
-      const __nv_bfloat16 v1 = __float2bfloat16_rn(vv_[e]);
-      vnew[lane + 32 * e] = bf16f(v1);
-      if (hg == 0) vdst[lane + 32 * e] = v1;
-    }
-  }
+  if (use_new && warp == kKvWarp) kv_row<D>(a, qraw, slot, p, cs, sn, knew, vnew, hg == 0);
 
   // ---- tiles with online softmax
   float m_run[HPC], l_run[HPC];
@@ -423,6 +430,25 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   pdl_trigger();
   pdl_wait();
   attn_unit<D, HPC>(a, blockIdx.x, blockIdx.y, blockIdx.z, asmem_k, 0, 1);
+}
+
+// K/V rows of an owning layer for every row of a step before its attention runs (prefill
+// blocks: rows of one sequence at consecutive positions read each other's keys, so no row
+// may append its own key inside the attention launch).  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(32) kv_write_kernel(const AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, lane = threadIdx.x;
+  const int p = __ldcg(a.positions + b), slot = __ldcg(a.slots + b);
+  if (p < 0 || p >= a.t_max || slot < 0 || slot >= a.max_batch) return;  // attention flags it
+  float cs[D / 64], sn[D / 64];
+#pragma unroll
+  for (int e = 0; e < D / 64; ++e) {
+    cs[e] = __ldg(a.rope_cos + (size_t)p * (D / 2) + lane + 32 * e);
+    sn[e] = __ldg(a.rope_sin + (size_t)p * (D / 2) + lane + 32 * e);
+  }
+  kv_row<D>(a, a.qkv + (size_t)b * a.qkv_stride, slot, p, cs, sn, nullptr, nullptr, true);
 }
 
 }  // namespace g4

@@ -127,6 +127,7 @@ struct g4_handle {
   float* trace = nullptr;
   int trace_stride = 0;
   // persistent step (n <= 2)
+  int rows = 0;  // activation rows the step buffers hold (>= max_batch)
   bool mega_ok = false;  // the persistent step was planned for this model
   bool mega_on = false;  // g4_set_step_mode(1): n_seq <= 2 steps run it
   MegaPhase* mega_phases = nullptr;
@@ -526,6 +527,10 @@ int attn_hpc(int nq, int nb) {
   (void)nb;
   return 1;
 }
+// Tokens per prefill block: one step over the rows of a prompt (the tensor-core GEMMs take up
+// to 64 rows).
+constexpr int kPrefillRows = 64;
+
 int attn_nsplit(int sms, int nq, int hpc, int nb, int max_keys) {
   const int n_hg = nq / hpc;
   int ns = cdiv(2 * sms, nb * n_hg);
@@ -564,9 +569,11 @@ struct ProfScope {
 // ------------------------------------------------------------------------------- the step
 g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens,
                         const int* d_idx, const int* d_pos, int* d_next, float* d_logits, bool stamps);
+// kv_first: write every row's K/V before the attention launch (prefill blocks, where rows of
+// one sequence at consecutive positions attend to each other's keys).
 g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens, const int* d_idx,
-                   const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr) {
-  if (h->mega_ok && h->mega_on && n <= 2 && !prof)
+                   const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr, bool kv_first = false) {
+  if (h->mega_ok && h->mega_on && n <= 2 && !prof && !kv_first)
     return run_step_mega(h, st, n, d_slots, d_tokens, d_idx, d_pos, d_next, d_logits, false);
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
@@ -645,7 +652,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.eps = eps;
       a.scale = Y.scale;
       a.window = Y.full ? 0 : c.sliding_window;
-      a.own = Y.own;
+      a.own = Y.own && !kv_first;
       a.kc = h->kc[Src.kv];
       a.vc = h->vc[Src.kv];
       a.t_max = c.max_context;
@@ -668,6 +675,14 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.counters = h->attn_cnt;
       a.err = h->err;
       ProfScope ps(prof, Y.full ? "attn.full" : "attn.sliding", 0.0);
+      if (kv_first && Y.own) {
+        switch (Y.d) {
+          case 64: launch(kv_write_kernel<64>, dim3(n), dim3(32), 0, st, a); break;
+          case 128: launch(kv_write_kernel<128>, dim3(n), dim3(32), 0, st, a); break;
+          case 256: launch(kv_write_kernel<256>, dim3(n), dim3(32), 0, st, a); break;
+          default: launch(kv_write_kernel<512>, dim3(n), dim3(32), 0, st, a); break;
+        }
+      }
       switch (Y.d) {
         case 64: launch_attn_d<64>(a, hpc, n, st); break;
         case 128: launch_attn_d<128>(a, hpc, n, st); break;
@@ -1269,8 +1284,10 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
     CK(cudaMemcpy(h->cos_t[t], cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
     CK(cudaMemcpy(h->sin_t[t], sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
   }
-  // activations
-  const int B = c.max_batch;
+  // activations: rows for a step of max_batch sequences or a prefill block of kPrefillRows
+  // tokens (rows of one sequence at consecutive positions)
+  const int B = std::max(c.max_batch, kPrefillRows);
+  h->rows = B;
   const int dmax = std::max(c.head_dim_full, c.head_dim_sliding);
   const int Fmax = std::max(c.mlp, c.mlp_shared);
   TRY(dalloc(h, &h->x0, (size_t)B * H));
@@ -1344,7 +1361,7 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   TRY(dalloc(h, &h->err, 1));
   CK(cudaMemsetAsync(h->err, 0, sizeof(int), st));
   TRY(dalloc(h, &h->step_next, B));
-  TRY(dalloc(h, &h->step_logits, (size_t)B * c.vocab));
+  TRY(dalloc(h, &h->step_logits, (size_t)B * c.vocab));  // only the rows that end a sequence are read
   CK(cudaStreamSynchronize(st));
   TRY(build_mega(h, st));
   return G4_OK;
@@ -1480,6 +1497,56 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
     if ((int64_t)start_pos[i] + len[i] > c.max_context) return G4_ERR_CONTEXT_OVERFLOW;
     order[i] = i;
   }
+  CK(cudaSetDevice(h->device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto upload = [&](const std::vector<int>& host) -> g4_status {
+    if (h->pf_cap < host.size()) {
+      if (h->pf_buf) { CK(cudaStreamSynchronize(st)); cudaFree(h->pf_buf); h->pf_buf = nullptr; h->pf_cap = 0; }
+      CK(cudaMalloc(&h->pf_buf, host.size() * sizeof(int)));
+      h->pf_cap = host.size();
+    }
+    CK(cudaMemcpyAsync(h->pf_buf, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice, st));
+    CK(cudaStreamSynchronize(st));  // the host staging vector goes out of scope afterwards
+    return G4_OK;
+  };
+  auto copy_out = [&](int q, int row, bool with_logits) -> g4_status {
+    CK(cudaMemcpyAsync(d_next_ids + q, h->step_next + row, sizeof(int), cudaMemcpyDeviceToDevice, st));
+    if (with_logits)
+      CK(cudaMemcpyAsync(d_logits + (size_t)q * c.vocab, h->step_logits + (size_t)row * c.vocab,
+                         (size_t)c.vocab * sizeof(float), cudaMemcpyDeviceToDevice, st));
+    return G4_OK;
+  };
+  if (!h->trace) {
+    // Blocks of up to kPrefillRows rows, sequence by sequence, positions ascending: each block
+    // is one step whose K/V rows are all written before its attention, so a row sees the keys
+    // of the earlier rows of its sequence in the same block.
+    int total = 0;
+    for (int i = 0; i < n_seq; ++i) total += len[i];
+    std::vector<int> host((size_t)3 * total);
+    std::vector<int> last(n_seq);
+    for (int i = 0, r = 0; i < n_seq; ++i) {
+      for (int t = 0; t < len[i]; ++t, ++r) {
+        host[(size_t)0 * total + r] = slots[i];
+        host[(size_t)1 * total + r] = start_pos[i] + t;
+        host[(size_t)2 * total + r] = offsets[i] + t;
+      }
+      last[i] = r - 1;  // the sequence's final row
+    }
+    TRY(upload(host));
+    for (int r0 = 0; r0 < total; r0 += kPrefillRows) {
+      const int n = std::min(kPrefillRows, total - r0);
+      bool ends = false;
+      for (int i = 0; i < n_seq; ++i) ends |= last[i] >= r0 && last[i] < r0 + n;
+      float* lg = (d_logits && ends) ? h->step_logits : nullptr;
+      TRY(run_step(h, st, n, h->pf_buf + r0, d_tokens, h->pf_buf + (size_t)2 * total + r0, h->pf_buf + (size_t)total + r0,
+                   h->step_next, lg, nullptr, true));
+      for (int i = 0; i < n_seq; ++i)
+        if (last[i] >= r0 && last[i] < r0 + n) TRY(copy_out(i, last[i] - r0, d_logits != nullptr));
+    }
+    return G4_OK;
+  }
+  // With a per-layer trace set: one decode step per prompt position (every active sequence
+  // one row), so the trace rows stay the sequences' rows.
   std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return len[a] > len[b]; });
   const int T = len[order[0]];
   // per step t: slots, positions, token indices of the active prefix of `order`
@@ -1497,15 +1564,7 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
     }
     n_act[t] = n;
   }
-  CK(cudaSetDevice(h->device));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (h->pf_cap < host.size()) {
-    if (h->pf_buf) { CK(cudaStreamSynchronize(st)); cudaFree(h->pf_buf); h->pf_buf = nullptr; h->pf_cap = 0; }
-    CK(cudaMalloc(&h->pf_buf, host.size() * sizeof(int)));
-    h->pf_cap = host.size();
-  }
-  CK(cudaMemcpyAsync(h->pf_buf, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice, st));
-  CK(cudaStreamSynchronize(st));  // the host staging vector goes out of scope below
+  TRY(upload(host));
   for (int t = 0; t < T; ++t) {
     const int n = n_act[t];
     const int* ds = h->pf_buf + ((size_t)0 * T + t) * n_seq;
@@ -1514,13 +1573,7 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
     const int n_next = t + 1 < T ? n_act[t + 1] : 0;  // sequences finishing now: [n_next, n)
     float* lg = (d_logits && n_next < n) ? h->step_logits : nullptr;
     TRY(run_step(h, st, n, ds, d_tokens, di, dp, h->step_next, lg));
-    for (int i = n_next; i < n; ++i) {
-      const int q = order[i];
-      CK(cudaMemcpyAsync(d_next_ids + q, h->step_next + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
-      if (d_logits)
-        CK(cudaMemcpyAsync(d_logits + (size_t)q * c.vocab, h->step_logits + (size_t)i * c.vocab,
-                           (size_t)c.vocab * sizeof(float), cudaMemcpyDeviceToDevice, st));
-    }
+    for (int i = n_next; i < n; ++i) TRY(copy_out(order[i], i, d_logits != nullptr));
   }
   return G4_OK;
 }

@@ -125,6 +125,10 @@ g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
  * 0.  d_next_ids[i] = greedy argmax after the sequence's last token; d_logits (nullable)
  * receives those logits [n_seq, vocab] fp32.  slots, offsets, start_pos are HOST arrays
  * (n_seq, n_seq + 1, n_seq entries); d_tokens is a DEVICE array of offsets[n_seq] ids.
+ * The prompt rows run in blocks of up to 64 (sequence by sequence, positions ascending): one
+ * step per block, with every row's K/V written before the block's attention, so a block's
+ * rows see each other's keys causally.  While a per-layer trace is set, one step per prompt
+ * position instead (trace rows are sequences).
  * Errors: G4_ERR_INVALID_ARG (n_seq outside 1..max_batch, empty or decreasing offsets, slot
  * out of range or repeated), G4_ERR_CONTEXT_OVERFLOW (start_pos + length > max_context). */
 g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_t* slots,

@@ -290,3 +290,26 @@ def test_step_mode_argument_checks(rt):
     dec.set_step_mode(0)
     assert dec.step_mode(1) == 0
     dec.close()
+
+
+def test_block_prefill_windows_and_ragged_lengths(rt):
+    """Prefill runs prompts in blocks of up to 64 rows whose K/V are written before the
+    block's attention: two sequences of 150 and 37 tokens (3 + 1 blocks, ragged tails, the
+    sliding window binding inside blocks) against the oracle, then decode steps."""
+    cfg = synth.get_config("tiny10")
+    w = synth.make_weights(cfg, "w4a16", seed=5, gain_std=0.1)
+    lens = [150, 37]
+    prompts = [synth.make_prompts(cfg["vocab"], 1, n, seed=40 + n)[0] for n in lens]
+    dec = rt.Decoder(cfg, w, max_batch=2, max_context=192)
+    nxt, lg = dec.prefill([0, 1], prompts, want_logits=True)
+    torch.cuda.synchronize()
+    got_ids, got = nxt.cpu().numpy(), lg.cpu().numpy()
+    assert dec.device_error()[1] == 0
+    for i, p in enumerate(prompts):
+        orc = oracle.Oracle(cfg, w, max_batch=1, max_context=192)
+        ref = orc.prefill([0], np.asarray(p)[None])[0]
+        assert np.max(np.abs(got[i] - ref)) <= LOGIT_TOL, i
+        top2 = np.sort(ref)[-2:]
+        if top2[1] - top2[0] > GAP_TIE:
+            assert got_ids[i] == int(np.argmax(ref)), i
+    dec.close()
