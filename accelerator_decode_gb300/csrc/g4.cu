@@ -127,7 +127,8 @@ struct g4_handle {
   float* trace = nullptr;
   int trace_stride = 0;
   // persistent step (n <= 2)
-  int rows = 0;  // activation rows the step buffers hold (>= max_batch)
+  int rows = 0;    // activation rows the step buffers hold (>= max_batch)
+  int l_tail = 0;  // layers [l_tail, num_layers) write no K/V
   bool mega_ok = false;  // the persistent step was planned for this model
   bool mega_on = false;  // g4_set_step_mode(1): n_seq <= 2 steps run it
   MegaPhase* mega_phases = nullptr;
@@ -570,9 +571,14 @@ struct ProfScope {
 g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens,
                         const int* d_idx, const int* d_pos, int* d_next, float* d_logits, bool stamps);
 // kv_first: write every row's K/V before the attention launch (prefill blocks, where rows of
-// one sequence at consecutive positions attend to each other's keys).
+// one sequence at consecutive positions attend to each other's keys).  n_keep >= 0: from the
+// first layer after which no layer writes K/V on, only rows keep_idx[0 .. n_keep) (their
+// slots and positions in keep_slots / keep_pos) go on: a prompt row that ends no sequence
+// feeds nothing past its last K/V write.  n_keep == 0 ends the step there.
 g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens, const int* d_idx,
-                   const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr, bool kv_first = false) {
+                   const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr, bool kv_first = false,
+                   const int* keep_idx = nullptr, const int* keep_slots = nullptr, const int* keep_pos = nullptr,
+                   int n_keep = -1) {
   if (h->mega_ok && h->mega_on && n <= 2 && !prof && !kv_first)
     return run_step_mega(h, st, n, d_slots, d_tokens, d_idx, d_pos, d_next, d_logits, false);
   const g4_config& c = h->cfg;
@@ -607,9 +613,25 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
   float* cur = h->x0;
   auto next_x = [&]() { return cur == h->xb[0] ? h->xb[1] : h->xb[0]; };
   const int ts = h->trace_stride;
+  const int l_tail = h->l_tail;
+  const float* rple = h->r_ple;  // residual branch entering the next layer
+  const float* ple_base = h->ple;
   for (int l = 0; l < L; ++l) {
     Layer& Y = h->layers[l];
     const int nqd = c.num_q_heads * Y.d;
+    if (l == l_tail && l > 0 && n_keep >= 0 && n_keep < n) {
+      if (n_keep == 0) return G4_OK;
+      float* xg = next_x();
+      launch(gather_rows_kernel, dim3(n_keep), dim3(256), 0, st, (const float*)cur, H, xg, H, keep_idx, H);
+      launch(gather_rows_kernel, dim3(n_keep), dim3(256), 0, st, (const float*)h->r_ple, H, h->r_mlp, H, keep_idx, H);
+      launch(gather_rows_kernel, dim3(n_keep), dim3(256), 0, st, ple_base, LP, h->pr, LP, keep_idx, LP);
+      cur = xg;
+      rple = h->r_mlp;
+      ple_base = h->pr;
+      d_slots = keep_slots;
+      d_pos = keep_pos;
+      n = n_keep;
+    }
     {  // QKV
       GemvIO io;
       io.x_in = cur;
@@ -621,12 +643,13 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       } else {
         const Layer& Pv = h->layers[l - 1];
         io.pro = PRO_RESID;
-        io.r_in = h->r_ple;
+        io.r_in = rple;
         io.r_stride = H;
         io.g_r = Pv.post_ple_norm;
         io.lambda = Pv.lambda;
         io.x_out = next_x();
       }
+      rple = h->r_ple;  // the gathered branch is used once
       io.y = h->qkv;
       io.y_stride = Y.qkv.n_valid;
       {
@@ -748,7 +771,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       io.x_out = next_x();
       io.y = h->pg;
       io.y_stride = P;
-      io.ple = h->ple + (size_t)l * P;
+      io.ple = ple_base + (size_t)l * P;
       io.ple_stride = LP;
       {
         ProfScope ps(prof, "gemv.ple_gate", (double)Y.pg.bytes);
@@ -1284,6 +1307,8 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
     CK(cudaMemcpy(h->cos_t[t], cs.data(), cs.size() * 4, cudaMemcpyHostToDevice));
     CK(cudaMemcpy(h->sin_t[t], sn.data(), sn.size() * 4, cudaMemcpyHostToDevice));
   }
+  h->l_tail = L;
+  while (h->l_tail > 0 && !h->layers[h->l_tail - 1].own) --h->l_tail;
   // activations: rows for a step of max_batch sequences or a prefill block of kPrefillRows
   // tokens (rows of one sequence at consecutive positions)
   const int B = std::max(c.max_batch, kPrefillRows);
@@ -1522,7 +1547,10 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
     // of the earlier rows of its sequence in the same block.
     int total = 0;
     for (int i = 0; i < n_seq; ++i) total += len[i];
-    std::vector<int> host((size_t)3 * total);
+    const int n_blocks = (total + kPrefillRows - 1) / kPrefillRows;
+    // [slots | positions | token indices] of all rows, then per block the rows that end a
+    // sequence: [kept row index | slot | position] x kPrefillRows
+    std::vector<int> host((size_t)3 * total + (size_t)n_blocks * 3 * kPrefillRows, 0);
     std::vector<int> last(n_seq);
     for (int i = 0, r = 0; i < n_seq; ++i) {
       for (int t = 0; t < len[i]; ++t, ++r) {
@@ -1532,16 +1560,34 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
       }
       last[i] = r - 1;  // the sequence's final row
     }
+    std::vector<std::vector<int>> kept(n_blocks);  // sequences whose final row is in the block
+    for (int i = 0; i < n_seq; ++i) kept[last[i] / kPrefillRows].push_back(i);
+    for (int k = 0; k < n_blocks; ++k) {
+      int* kb = host.data() + (size_t)3 * total + (size_t)k * 3 * kPrefillRows;
+      for (size_t j = 0; j < kept[k].size(); ++j) {
+        const int i = kept[k][j];
+        kb[j] = last[i] - k * kPrefillRows;
+        kb[kPrefillRows + j] = slots[i];
+        kb[2 * kPrefillRows + j] = start_pos[i] + len[i] - 1;
+      }
+    }
     TRY(upload(host));
-    for (int r0 = 0; r0 < total; r0 += kPrefillRows) {
-      const int n = std::min(kPrefillRows, total - r0);
-      bool ends = false;
-      for (int i = 0; i < n_seq; ++i) ends |= last[i] >= r0 && last[i] < r0 + n;
-      float* lg = (d_logits && ends) ? h->step_logits : nullptr;
+    for (int k = 0; k < n_blocks; ++k) {
+      const int r0 = k * kPrefillRows, n = std::min(kPrefillRows, total - r0);
+      const int* kb = h->pf_buf + (size_t)3 * total + (size_t)k * 3 * kPrefillRows;
+      // compaction needs a K/V-free tail after layer 0; otherwise every row runs to the end
+      const bool tail = h->l_tail > 0 && h->l_tail < c.num_layers;
+      const int n_keep = (int)kept[k].size();
+      float* lg = (d_logits && n_keep > 0) ? h->step_logits : nullptr;
       TRY(run_step(h, st, n, h->pf_buf + r0, d_tokens, h->pf_buf + (size_t)2 * total + r0, h->pf_buf + (size_t)total + r0,
-                   h->step_next, lg, nullptr, true));
-      for (int i = 0; i < n_seq; ++i)
-        if (last[i] >= r0 && last[i] < r0 + n) TRY(copy_out(i, last[i] - r0, d_logits != nullptr));
+                   h->step_next, lg, nullptr, true, kb, kb + kPrefillRows, kb + 2 * kPrefillRows, tail ? n_keep : -1));
+      // rows kept past the K/V layers come out in kept order (ascending rows); without a
+      // compaction (no K/V-free tail) they stay at their block rows
+      const bool compacted = tail && n_keep < n;
+      for (int j = 0; j < n_keep; ++j) {
+        const int i = kept[k][j];
+        TRY(copy_out(i, compacted ? j : last[i] - r0, d_logits != nullptr));
+      }
     }
     return G4_OK;
   }

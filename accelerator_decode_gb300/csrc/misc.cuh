@@ -73,6 +73,18 @@ __global__ void ple_combine_kernel(const float* pr, const float* tok, const __nv
   }
 }
 
+// Row gather for prefill blocks: dst row i = src row idx[i] (width floats, a multiple of 4;
+// strides in floats, multiples of 4).  dst and src must not overlap.
+__global__ void gather_rows_kernel(const float* src, int src_stride, float* dst, int dst_stride, const int* idx,
+                                   int width) {
+  pdl_trigger();
+  pdl_wait();
+  const int i = blockIdx.x;
+  const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)__ldcg(idx + i) * src_stride);
+  float4* d4 = reinterpret_cast<float4*>(dst + (size_t)i * dst_stride);
+  for (int c = threadIdx.x; c < width / 4; c += blockDim.x) d4[c] = __ldcg(s4 + c);
+}
+
 // ------------------------------------------------------------------------------ repacking
 // One destination 32-row block: `w` points at its first source row (nullptr = zero block),
 // `s` at its first scale row (W4A16), `rows` valid rows (<= 32).
