@@ -389,6 +389,90 @@ def run_gpu(args, wl, cfg, fmt):
     return result
 
 
+# ------------------------------------------------------------------------- agent replay
+def run_replay(args, wl, cfg, fmt):
+    """Agent replay: `batch` sequences start at a `prompt`-token context; each of `turns` turns
+    appends the previous turn's last output (not yet in the cache) and `turn_append` fresh
+    ids by append-prefill, then runs `out` - 1 decode steps.  Reports decode tok/s per turn
+    against the context length (CUDA events on the decode steps of each turn)."""
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    from accelerator_decode_gb300.runtime import Decoder
+
+    B, n_out, turns = wl["batch"], wl["out"], wl["turns"]
+    sched = synth.replay_schedule(start=wl["prompt"], end=wl["prompt"] + turns * wl["turn_append"], turns=turns,
+                                  outputs=n_out)
+    max_ctx = sched[0][0] + sum(a + o for a, o in sched[1:])
+    max_ctx = ((max_ctx + 63) // 64) * 64
+    weights = synth.make_weights(cfg, fmt, seed=args.seed)
+    dec = Decoder(cfg, weights, max_batch=B, max_context=max_ctx, device=local)
+    dev = torch.device("cuda", local)
+    st = torch.cuda.Stream()
+    slots = list(range(B))
+    ctx = [0] * B
+    last = None
+    rows, dec_tokens, dec_ms = [], 0, 0.0
+    clocks = ClockSampler(local)
+    clocks.start()
+    with torch.cuda.stream(st):
+        d_slots = torch.arange(B, dtype=torch.int32, device=dev)
+        tok = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
+        pos = torch.empty(B, dtype=torch.int32, device=dev)
+        for turn, (fresh, outs) in enumerate(sched):
+            ids = synth.make_prompts(cfg["vocab"], B, fresh, seed=args.seed + 1000 + turn, stream=rank)
+            if last is not None:
+                ids = np.concatenate([last[:, None], ids], axis=1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            nxt, _ = dec.prefill(slots, list(ids), start_pos=list(ctx), stream=st)
+            e1.record(st)
+            st.synchronize()
+            pf_ms = e0.elapsed_time(e1)
+            ctx = [c + ids.shape[1] for c in ctx]
+            if outs == 0:
+                continue
+            tok[0].copy_(nxt)
+            pos.fill_(ctx[0])
+            steps = outs - 1
+            d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            d0.record(st)
+            for i in range(steps):
+                dec.decode_step(d_slots, tok[i % 2], pos, tok[(i + 1) % 2], None, stream=st)
+                pos.add_(1)
+            d1.record(st)
+            d1.synchronize()
+            ms = d0.elapsed_time(d1)
+            rows.append({"context": ctx[0], "decode_tok_s": round(B * steps / (ms / 1e3), 1),
+                         "prefill_tok_s": round(B * ids.shape[1] / (pf_ms / 1e3), 1)})
+            dec_tokens += B * steps
+            dec_ms += ms
+            ctx = [c + steps for c in ctx]
+            last = tok[steps % 2].cpu().numpy().astype(np.int32)
+        status, word = dec.device_error(stream=st)
+    clk = clocks.stop()
+    dec.close()
+    return {
+        "metric": METRIC + " (agent replay: decode tok/s versus context)",
+        "value": round(dec_tokens / (dec_ms / 1e3), 2),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": dec_tokens // B,
+        "warmup": 0,
+        "ms_per_step": round(dec_ms / max(1, dec_tokens // B), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl["name"], "weights": fmt, "batch_per_gpu": B, "start_context": sched[0][0],
+                   "final_context": ctx[0], "turns": turns, "outputs_per_turn": n_out},
+        "by_context": rows,
+        "clocks": clk,
+        "device_error": word,
+    }
+
+
 # ------------------------------------------------------------------------- reference arm
 def run_reference(args, wl, cfg, fmt):
     rank, world, _ = dist_env()
@@ -448,6 +532,8 @@ def main(argv=None):
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
     if args.impl == "reference":
         res = run_reference(args, wl, cfg, fmt)
+    elif "turns" in wl:
+        res = run_replay(args, wl, cfg, fmt)
     else:
         res = run_gpu(args, wl, cfg, fmt)
     if res is not None and rank == 0:
