@@ -1,4 +1,4 @@
-// Weight-only projections for batches >= 16 on the 5th-generation tensor cores (tcgen05).
+// Weight-only projections for batches >= 5 on the 5th-generation tensor cores (tcgen05).
 //
 // D[n, b] = sum_k W[n, k] x[b, k] with the weight rows as the MMA's M (128 per CTA) and the
 // padded batch as N ("swap AB").  Per 64-wide k-block:

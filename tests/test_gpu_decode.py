@@ -188,7 +188,8 @@ def test_ragged_batch_slots_and_append(rt):
 
 
 def test_batch_larger_than_gemv_chunk(rt):
-    """Batch 6 crosses the 4-row GEMV chunk; every sequence must match its oracle run."""
+    """Batch 6 (past the 4-row GEMV pass: the tensor-core path); every sequence must match its
+    oracle run."""
     cfg = synth.get_config("tiny")
     w = synth.make_weights(cfg, "w4a16", seed=9)
     prompts = synth.make_prompts(cfg["vocab"], 6, 8, seed=6)
