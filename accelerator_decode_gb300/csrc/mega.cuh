@@ -1,7 +1,6 @@
-// Persistent decode step for 1-2 sequences: one cooperative launch runs the whole step as a
-// static program of phases separated by grid barriers.  It removes the ~250 kernel
-// boundaries of the launch-per-phase path, which at batch 1 cost more than the 1.87 GB of
-// weights take to stream.
+// Persistent decode step for 1-2 sequences: one cooperative launch (one CTA per SM) runs the
+// whole step as a static program of phases separated by grid barriers, in place of the ~250
+// kernel boundaries of the launch-per-phase path.
 //
 // Phases (the same arithmetic as the launch-per-phase path, see g4.cu):
 //   PMP      pr parts = W_pmp (E[t] sqrt H)                       (K slices -> partials)
@@ -11,15 +10,19 @@
 //            (x0 = E[t] sqrt H), then RMSNorm.  Output: final rows (with the GeGLU / PLE
 //            epilogue) or raw K-slice partials, which the next residual update sums in
 //            slice order.
-//   ATTN     flash-decode units (attn_unit), two per CTA (one per 128-thread half)
-//   LMHEAD   final residual + RMSNorm, logits rows, running argmax per CTA
+//   ATTN     flash-decode units (attn_unit), two per CTA (one per 128-thread half; one for
+//            head dim 512)
+//   LMHEAD   final residual + RMSNorm, logits rows, running argmax per CTA (a projection
+//            phase with an argmax epilogue)
 //   ARGMAX   CTA 0 reduces the per-CTA argmax partials
-// Units of a GEMV phase are (row group, K slice of spu supergroups); a CTA runs upc units
-// at once with wpu warps each (upc * wpu = 8).  The grid barrier is a monotonically
+// Units of a projection phase are (row group, K slice of spu supergroups), dealt round-robin
+// to the CTAs; the CTA's eight warps share each unit's tiles.  Their weights arrive through
+// the shared-memory weight ring (see MegaRing below).  The grid barrier is a monotonically
 // increasing counter (cleared before the launch); its wait is bounded: on expiry a CTA sets
-// the timeout bit and the abort flag, and every CTA leaves at its next barrier.
-// Visibility: data written by other CTAs earlier in the launch is read only through L2 (cp.async.cg,
-// ld.global.cg) or after the barrier's acquire fence, never from a possibly stale L1 line.
+// the timeout bit and the abort flag, and every CTA leaves at its next wait.
+// Visibility: data written by other CTAs earlier in the launch is read only through L2
+// (cp.async.cg, ld.global.cg) or after the barrier's acquire fence, never from a possibly
+// stale L1 line.
 #pragma once
 #include "attn.cuh"
 #include "common.cuh"
