@@ -383,10 +383,49 @@ def run_gpu(args, wl, cfg, fmt):
                                   "sample": f"{n} oracle decode steps of batch {ob} at positions 1..{n} "
                                             f"({dt:.1f} s), same weights"}
     dec.close()
+    if args.batch64 and B == 1 and world == 1:
+        result["batch64"] = batch64_line(args, cfg, weights, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return result
+
+
+def batch64_line(args, cfg, weights, local):
+    """Companion figure for the metric's batch-64 half: the same model and weights at 64
+    sequences (128-token prompts), W >= 3 warm-up steps, 64 timed steps with CUDA events on
+    the launching stream; inputs (1.9+ GB of weights per step) exceed L2."""
+    import torch
+    from accelerator_decode_gb300.runtime import Decoder
+    B, P0, K, W = 64, 128, 64, max(3, min(args.warmup, 8))
+    dev = torch.device("cuda", local)
+    dec = Decoder(cfg, weights, max_batch=B, max_context=((P0 + K + W + 1 + 63) // 64) * 64, device=local)
+    prompts = synth.make_prompts(cfg["vocab"], B, P0, seed=args.seed)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        nxt, _ = dec.prefill(list(range(B)), list(prompts), stream=st)
+        slots = torch.arange(B, dtype=torch.int32, device=dev)
+        tok = [nxt.clone(), torch.empty_like(nxt)]
+        pos = torch.full((B,), P0, dtype=torch.int32, device=dev)
+        for i in range(W + K):
+            if i == W:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                st.synchronize()
+                e0.record(st)
+            dec.decode_step(slots, tok[i % 2], pos, tok[(i + 1) % 2], None, stream=st)
+            pos.add_(1)
+        e1.record(st)
+        e1.synchronize()
+        status, word = dec.device_error(stream=st)
+    ms = e0.elapsed_time(e1) / K
+    dec.close()
+    wbytes, kvbytes = algorithmic_bytes(cfg, weights["fmt"], B, [P0 + W + i for i in range(K)])
+    peak, peak_src = measured_peak()
+    return {"value": round(B / (ms / 1e3), 2), "unit": "tok/s", "ms_per_step": round(ms, 5), "steps": K, "warmup": W,
+            "batch": B, "prompt_tokens": P0,
+            "step_roofline": {"bytes_per_step": wbytes + kvbytes, "frac": round((wbytes + kvbytes) / (ms / 1e3) / 1e9 / peak, 4),
+                              "peak": peak, "peak_source": peak_src},
+            "device_error": word}
 
 
 # ------------------------------------------------------------------------- agent replay
@@ -520,6 +559,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-batch64", dest="batch64", action="store_false",
+                    help="skip the batch-64 companion figure of the batch-1 workload")
     ap.add_argument("--impl-check-only", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args.warmup < 3:
