@@ -15,7 +15,11 @@
 //     gemv ple_proj  r_ple = W_pp g
 //   gemv lm_head     prologue x = (x + RMSNorm(r_ple)) lambda; y = RMSNorm(x); logits = E y,
 //                    block argmax + last-block reduction -> next ids
-// Decode steps are captured into a CUDA graph per (n, pointer set) and replayed.
+// "gemv" is the tiled GEMV for up to 4 rows and the tcgen05 GEMM (with an activation-prep
+// kernel for the prologue) from 5 rows.  Decode steps are captured into a CUDA graph per
+// (n, step mode, pointer set) and replayed; g4_set_step_mode(1) runs steps of 1-2 rows as one
+// persistent launch instead (mega.cuh).  Prefill runs blocks of up to 64 prompt rows through
+// the same step with the K/V rows written ahead of each attention (kv_first).
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
