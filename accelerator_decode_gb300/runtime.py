@@ -31,6 +31,9 @@ class Decoder:
     """One libg4 handle.  `weights` is a host weight dict in the canonical format (synth)."""
 
     def __init__(self, cfg, weights, max_batch, max_context, device=0):
+        if isinstance(weights["embed"], dict) or isinstance(weights["ple_table"], dict):
+            raise ValueError("g4_create takes bf16 vocabulary tables (token embedding and "
+                             "per-layer table); int4 tables are not supported by the library")
         self.cfg = cfg
         self.device = torch.device("cuda", device)
         self.max_batch, self.max_context = max_batch, max_context

@@ -6,6 +6,8 @@ Sources (page title, section):
   [P1] "Gemma 4 E2B in JAX on One TPU v5e: bf16 or 4-Bit, Python or Rust, and How It Stands
        Against vLLM" -- Step 2 (jitted prefill, static KV cache, one decode step per token),
        Step 3 (W4A16 weights unpacked before every matmul), Step 4 (the Rust rms_norm).
+  [P2] "Six serving engines on one Cloud TPU v5e chip (Gemma 4 E2B)" -- What Changes and
+       What Stays, Step 3 (a build with the vocabulary tables and the lm_head in int4).
   [P3] "Porting Gemma 4 E2B to SGLang-JAX on One Cloud TPU v5e" -- Step 1 (config and layer
        pattern), Step 3 (per-layer embeddings: construction and per-layer mixing), Step 4 (a
        sharing layer applies RoPE to its queries only and reads its source's post-norm,
@@ -14,11 +16,20 @@ Sources (page title, section):
        Repack" -- cell 2.2 (tied lm_head, 276 packed linears), cell 3.1 (int4 groups of 32).
   [P5] "One TPU chip, eight agents" -- The engine (kv_share_map, static cache, cached decode
        against a full re-forward, RoPE on logical position), Feasibility part 1 (18 KiB of KV
-       per token), Two optimizations that didn't work (decode dequantises to bf16 and reads
-       the full weight set per token).
+       per token; resident-token ceilings at bf16 and int8), Measured: the raw JAX decode
+       kernel (int8 KV cache; the per-layer table in int4: weight tree 6.618 -> 3.113 GB),
+       Two optimizations that didn't work (decode dequantises to bf16 and reads the full
+       weight set per token).
 
 What pins each part (tests/test_oracle_*.py):
-  dequant_w4a16    hand-built groups with exact values, nibble-order probes, RNE ties
+  dequant_w4a16    hand-built groups with exact values, nibble-order probes, RNE ties,
+                   groups of 256 (the per-layer table's one scale per layer slice)
+  kv_int8_*        exact codes for rows on a power-of-two grid, half-even ties, the s/2
+                   error bound, zero rows, power-of-two scale invariance; bytes per token
+                   against the printed bf16 / int8 resident-token ceilings
+  int4 tables      tables whose int4 values are exact bf16 numbers decode identically to
+                   the bf16 tables; the per-layer table's bytes against the printed weight
+                   tree before and after its int4 quantisation
   rmsnorm          constant vectors, scale invariance, a hand-computed case
   gelu_tanh        closed-form values and its distance to the erf GELU
   rope             identity at position 0, norm preservation, relative-position property
@@ -66,23 +77,62 @@ def bf16_round(x):
 
 
 def dequant_w4a16(packed, scales, dtype=np.float32):
-    """W4A16 -> dense weights: W[n, k] = bf16(q[n, k] * s[n, k // 32]).
+    """W4A16 -> dense weights: W[n, k] = bf16(q[n, k] * s[n, k // G]).
 
     packed: int32 [N, K/8]; element k in word k // 8, bits 4*(k % 8).., two's complement.
-    scales: bf16 bits [N, K/32].  The product q*s is exact (4-bit integer times an 8-bit
-    significand); it is then rounded to bf16 as dequantising to bf16 does [P5, Two
-    optimizations; P4, cell 1.2]."""
+    scales: bf16 bits [N, K/G]; the group size G = K / scales.shape[1] is 32 for the linears
+    and the token embedding, 256 (one scale per layer slice) for the per-layer table.  The
+    product q*s is exact (4-bit integer times an 8-bit significand); it is then rounded to
+    bf16 as dequantising to bf16 does [P5, Two optimizations; P4, cell 1.2]."""
     packed = np.asarray(packed)
     n_out, words = packed.shape
+    scales = np.asarray(scales)
+    assert (words * 8) % scales.shape[1] == 0
+    group = (words * 8) // scales.shape[1]
     u = packed.view(np.uint32)
     shifts = np.arange(8, dtype=np.uint32) * np.uint32(4)
     nib = (u[:, :, None] >> shifts) & np.uint32(0xF)
     q = nib.astype(np.int32).reshape(n_out, words * 8)
     q = np.where(q >= 8, q - 16, q)
     s = bf16_bits_to_float(scales, np.float64)
-    s = np.repeat(s, 32, axis=1)
+    s = np.repeat(s, group, axis=1)
     prod = q.astype(np.float64) * s                    # exact
     return bf16_round(prod).astype(dtype)
+
+
+def table_rows(table, rows, dtype=np.float32):
+    """Rows of a vocabulary table (token embedding or per-layer table): bf16 bits [V, n], or
+    an int4 table {"packed", "scales"} dequantised row by row [P2, Step 3: the vocabulary
+    tables in int4 too; P5, Measured: the per-layer table quantised to int4]."""
+    if isinstance(table, dict):
+        return dequant_w4a16(table["packed"][rows], table["scales"][rows], dtype)
+    return bf16_bits_to_float(table[rows], dtype)
+
+
+# ----------------------------------------------------------------------------------------
+# int8 KV rows
+# ----------------------------------------------------------------------------------------
+
+
+def kv_int8_quantize(v):
+    """Symmetric int8 code of each K or V row (last axis) [P5, Measured: int8 KV cache].
+
+    The pages give no granularity; the reading is one fp32 scale per stored row (one
+    position of one layer's single KV head, K and V separately), taken in fp32:
+      a = max_j |v_j|,  s = a / 127,  c_j = round_half_even(v_j / s) clipped to [-127, 127];
+    an all-zero row has s = 0 and codes 0.  Returns (codes int8 [..., d], s fp32 [..., 1])."""
+    v = np.asarray(v).astype(np.float32)
+    a = np.max(np.abs(v), axis=-1, keepdims=True)
+    s = a / np.float32(127.0)
+    safe = np.where(s > 0, s, np.float32(1.0))
+    c = np.rint(v / safe)
+    c = np.where(s > 0, np.clip(c, -127, 127), 0)
+    return c.astype(np.int8), s.astype(np.float32)
+
+
+def kv_int8_dequantize(codes, s, dtype=np.float32):
+    """Stored value of an int8 row: c_j * s, formed in fp32 (exact in fp64)."""
+    return (codes.astype(np.float32) * s.astype(np.float32)).astype(dtype)
 
 
 # ----------------------------------------------------------------------------------------
@@ -218,11 +268,20 @@ def param_counts(cfg):
     )
 
 
-def kv_bytes_per_token(cfg, copy_to_every_layer=False):
-    """bf16 K+V bytes per token: one KV head per layer that keeps a cache."""
+def kv_bytes_per_token(cfg, copy_to_every_layer=False, kv_dtype="bf16"):
+    """K+V bytes per token: one KV head per layer that keeps a cache; bf16 values, or int8
+    codes plus one fp32 scale per row."""
     own = owns_kv(cfg)
     layers = range(cfg["num_layers"]) if copy_to_every_layer else [l for l in range(cfg["num_layers"]) if own[l]]
+    if kv_dtype == "int8":
+        return sum(2 * cfg["num_kv_heads"] * (head_dim(cfg, l) + 4) for l in layers)
+    assert kv_dtype == "bf16"
     return sum(2 * 2 * cfg["num_kv_heads"] * head_dim(cfg, l) for l in layers)
+
+
+def int4_table_bytes(n_rows, n_cols, group):
+    """Bytes of a vocabulary table in int4: half a byte per value plus a bf16 scale per group."""
+    return n_rows * n_cols // 2 + 2 * (n_rows * n_cols // group)
 
 
 # ----------------------------------------------------------------------------------------
@@ -231,13 +290,14 @@ def kv_bytes_per_token(cfg, copy_to_every_layer=False):
 
 
 class Oracle:
-    """Greedy decoder over a per-sequence static KV cache (bf16 K/V, one KV head).
+    """Greedy decoder over a per-sequence static KV cache (bf16 or int8 K/V, one KV head).
 
     Per token id t at position p [P3, Steps 3-5; P5, The engine]:
       x = E[t] * sqrt(H)
       tok = T_ple[t] * sqrt(P); pr = RMSNorm((W_pmp x) * H^-1/2 per P-chunk); ple = (pr + tok) / sqrt 2
       per layer l: h = RMSNorm(x); q = RoPE(RMSNorm_head(W_q h)); K/V-owning layers store
-        bf16(RoPE(RMSNorm_head(W_k h))) and bf16(W_v h) at slot p; attention over the visible
+        RoPE(RMSNorm_head(W_k h)) and W_v h at slot p, as bf16 or as int8 rows (kv_dtype);
+        E and T_ple are bf16 tables or int4 tables dequantised on use; attention over the visible
         keys of the source layer's cache; x += RMSNorm(W_o o);
         m = RMSNorm(x); x += RMSNorm(W_d (gelu(W_g m) * (W_u m)));
         x += RMSNorm(W_pp (gelu(W_pg x) * ple_l)); x *= lambda_l
@@ -245,7 +305,9 @@ class Oracle:
     """
 
     def __init__(self, cfg, weights, max_batch=1, max_context=None, dtype=np.float32,
-                 workers=None):
+                 workers=None, kv_dtype="bf16"):
+        assert kv_dtype in ("bf16", "int8")
+        self.kv_dtype = kv_dtype
         self.cfg = cfg
         self.dtype = dt = np.dtype(dtype)
         self.t = dt.type
@@ -279,8 +341,8 @@ class Oracle:
         with ThreadPoolExecutor(nw) as ex:
             mats = list(ex.map(lambda j: lin(j[1]), jobs))
         self.W = {k: m for (k, _), m in zip(jobs, mats)}
-        self.E = bf16_bits_to_float(weights["embed"], dt)
-        self.ple_table = weights["ple_table"]            # bf16 bits; rows gathered per token
+        self.E = table_rows(weights["embed"], slice(None), dt)   # also the tied lm_head
+        self.ple_table = weights["ple_table"]            # bf16 bits or int4; rows gathered per token
         self.g_ppn = gain(weights["ple_proj_norm"])
         self.g_final = gain(weights["final_norm"])
         self.lw = []
@@ -305,7 +367,8 @@ class Oracle:
 
     # -- cache ------------------------------------------------------------------------------
     def reset(self):
-        """Fresh cache: per owning layer K and V [max_batch, max_context, d] of bf16 values."""
+        """Fresh cache: per owning layer K and V [max_batch, max_context, d] of stored values
+        (bf16 numbers, or int8 codes times their row scale)."""
         self.K, self.Vc = {}, {}
         for l in range(self.L):
             if self.own[l]:
@@ -316,7 +379,7 @@ class Oracle:
     # -- pieces -----------------------------------------------------------------------------
     def embed(self, tokens):
         x = self.E[tokens] * self.sqrt_h
-        tok = bf16_bits_to_float(self.ple_table[tokens], self.dtype) * self.sqrt_p
+        tok = table_rows(self.ple_table, tokens, self.dtype) * self.sqrt_p
         tok = tok.reshape(len(tokens), self.L, self.P)
         pr = (x @ self.W["pmp"].T) * self.inv_sqrt_h
         pr = rmsnorm(pr.reshape(len(tokens), self.L, self.P), self.g_ppn, self.eps)
@@ -338,7 +401,13 @@ class Oracle:
         k = (h @ self.W[(l, "k")].T).reshape(n, 1, d)
         k = apply_rope(rmsnorm(k, g["k_norm"], self.eps), cp, sp)[:, 0]
         v = h @ self.W[(l, "v")].T
-        return q, bf16_round(k), bf16_round(v)
+        return q, self._stored(k), self._stored(v)
+
+    def _stored(self, r):
+        """The value a cache row holds: bf16(r), or its int8 code times its scale."""
+        if self.kv_dtype == "int8":
+            return kv_int8_dequantize(*kv_int8_quantize(r), dtype=self.dtype)
+        return bf16_round(r)
 
     def _mlp_ple(self, l, x, ple_l):
         g = self.lw[l]

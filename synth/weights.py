@@ -5,6 +5,8 @@ Draws (the synthetic workloads' recipe):
     embedding table): N(0, std) drawn in fp32, rounded to bf16 round-to-nearest-even.
   * W4A16 linears: q ~ uniform integers in [-8, 7]; scale = bf16(|N(0, scale_std)|), one per
     32 input values; packed eight nibbles per int32, low nibble first.
+  * int4 vocabulary tables (optional): drawn the same way, one scale per 32 values of an
+    embedding row and one per 256-wide layer slice of a per-layer-table row.
   * RMSNorm gains: bf16(1 + N(0, gain_std)), i.e. exactly 1 at gain_std = 0; the query and
     key norms' gains are bf16(qk_gain * that) (qk_gain = 1 leaves them unchanged).
   * layer scales: 1 + N(0, layer_scale_std) in fp32 (exactly 1 at std 0).
@@ -73,14 +75,14 @@ def _scaled_gain(g, factor):
     return bf16_from_f32(np.float32(factor) * (g.astype(np.uint32) << np.uint32(16)).view(np.float32))
 
 
-def _int4_linear(n_out, n_in, scale_std, seed, tid, pool):
-    assert n_in % 32 == 0
+def _int4_linear(n_out, n_in, scale_std, seed, tid, pool, group=32):
+    assert n_in % group == 0 and group % 8 == 0
     q = np.empty(n_out * n_in, np.int8)
     _chunked(q.size, seed, tid, lambda rng, m: rng.integers(-8, 8, m, dtype=np.int8), q, pool)
     nib = (q.reshape(n_out, n_in // 8, 8).astype(np.uint32) & np.uint32(0xF))
     shifts = (np.arange(8, dtype=np.uint32) * np.uint32(4))
     packed = np.bitwise_or.reduce(nib << shifts, axis=2).view(np.int32)
-    s = np.empty(n_out * (n_in // 32), np.uint16)
+    s = np.empty(n_out * (n_in // group), np.uint16)
 
     def fill(rng, m):
         a = np.abs(rng.standard_normal(m, dtype=np.float32))
@@ -88,7 +90,7 @@ def _int4_linear(n_out, n_in, scale_std, seed, tid, pool):
         return bf16_from_f32(a)
 
     _chunked(s.size, seed, tid + 50_000, fill, s, pool)
-    return {"packed": np.ascontiguousarray(packed), "scales": s.reshape(n_out, n_in // 32),
+    return {"packed": np.ascontiguousarray(packed), "scales": s.reshape(n_out, n_in // group),
             "shape": (n_out, n_in)}
 
 
@@ -107,16 +109,18 @@ def linear_shapes(cfg, layer):
 
 
 def make_weights(cfg, fmt, seed=0, std=0.02, scale_std=0.004, gain_std=0.0,
-                 layer_scale_std=0.0, embed_std=None, qk_gain=1.0):
+                 layer_scale_std=0.0, embed_std=None, qk_gain=1.0, tables="bf16"):
     """Draw every tensor of the synthetic checkpoint.
 
-    fmt: "bf16" (every linear bf16) or "w4a16" (linears int4 + bf16 group scales; the token
-    embedding and per-layer-embedding table stay bf16).  K and V projections are drawn for
+    fmt: "bf16" (every linear bf16) or "w4a16" (linears int4 + bf16 group scales).
+    tables: "bf16" (token embedding and per-layer-embedding table N(0, embed_std) in bf16) or
+    "int4" (both drawn like the int4 linears: the embedding with a scale per 32 values, the
+    per-layer table with one scale per 256-wide layer slice).  K and V projections are drawn for
     every layer, as a checkpoint that carries them everywhere would; a decoder reads those
     of the layers that compute their own K/V.  qk_gain < 1 softens the attention scores
     (they scale with qk_gain squared), which keeps deep random models well conditioned.
     """
-    assert fmt in ("bf16", "w4a16")
+    assert fmt in ("bf16", "w4a16") and tables in ("bf16", "int4")
     L, H, P, V = cfg["num_layers"], cfg["hidden"], cfg["ple_dim"], cfg["vocab"]
     estd = std if embed_std is None else embed_std
     with _pool() as pool:
@@ -126,9 +130,15 @@ def make_weights(cfg, fmt, seed=0, std=0.02, scale_std=0.004, gain_std=0.0,
                         "shape": (n_out, n_in)}
             return _int4_linear(n_out, n_in, scale_std, seed, tid, pool)
 
-        w = {"fmt": fmt,
-             "embed": _normal_bf16((V, H), estd, seed, 1, pool),
-             "ple_table": _normal_bf16((V, L * P), estd, seed, 2, pool),
+        if tables == "bf16":
+            embed = _normal_bf16((V, H), estd, seed, 1, pool)
+            ple_table = _normal_bf16((V, L * P), estd, seed, 2, pool)
+        else:
+            embed = _int4_linear(V, H, scale_std, seed, 1, pool)
+            ple_table = _int4_linear(V, L * P, scale_std, seed, 2, pool, group=P)
+        w = {"fmt": fmt, "tables": tables,
+             "embed": embed,
+             "ple_table": ple_table,
              "ple_model_proj": linear(L * P, H, 3),
              "ple_proj_norm": _gain_bf16(P, gain_std, seed, 4, pool),
              "final_norm": _gain_bf16(H, gain_std, seed, 5, pool),

@@ -120,3 +120,82 @@ def test_fp32_tracks_fp64(tiny):
 def test_argmax_lowest_index_on_ties():
     x = np.array([[0.0, 3.0, 1.0, 3.0], [5.0, 5.0, 5.0, 5.0]])
     assert oracle.greedy_argmax(x).tolist() == [1, 0]
+
+
+def _pack_int4(q):
+    """[N, K] integers in [-8, 7] -> int32 [N, K/8], low nibble first (canonical layout)."""
+    nib = (np.asarray(q).reshape(q.shape[0], -1, 8) & 0xF).astype(np.uint32)
+    return np.bitwise_or.reduce(nib << (np.arange(8, dtype=np.uint32) * np.uint32(4)), axis=2).view(np.int32)
+
+
+def test_int4_tables_holding_bf16_numbers_decode_as_those_bf16_tables():
+    """Vocabulary tables in int4 (Six serving engines, Step 3; One TPU chip, eight agents,
+    Measured): when every q * s is a bf16 number, the int4 tables must decode exactly as bf16
+    tables holding those numbers -- the embedding gather, the per-layer rows and the tied
+    lm_head all read the dequantised table, with the per-layer table's one scale per slice."""
+    cfg = synth.get_config("tiny10")
+    w = synth.make_weights(cfg, "w4a16", seed=3, gain_std=0.1, layer_scale_std=0.1)
+    rng = np.random.default_rng(7)
+    w4, wb = dict(w, tables="int4"), dict(w)
+    V, H, P, L = cfg["vocab"], cfg["hidden"], cfg["ple_dim"], cfg["num_layers"]
+    for name, cols, group in (("embed", H, 32), ("ple_table", L * P, P)):
+        q = rng.integers(-8, 8, (V, cols))
+        e = rng.integers(-9, -5, (V, cols // group)).astype(np.float64)
+        s = np.exp2(e)                                   # powers of two: q * s is exact in bf16
+        w4[name] = {"packed": _pack_int4(q), "scales": synth.bf16_from_f32(s.astype(np.float32)),
+                    "shape": (V, cols)}
+        wb[name] = synth.bf16_from_f32((q * np.repeat(s, group, axis=1)).astype(np.float32))
+    pr = synth.make_prompts(V, 1, 12, seed=4)
+    for kv in ("bf16", "int8"):
+        ra = oracle.Oracle(cfg, w4, 1, 32, np.float64, kv_dtype=kv).generate(pr, 5, keep_logits=True)
+        rb = oracle.Oracle(cfg, wb, 1, 32, np.float64, kv_dtype=kv).generate(pr, 5, keep_logits=True)
+        np.testing.assert_array_equal(ra["logits"], rb["logits"])
+        np.testing.assert_array_equal(ra["tokens"], rb["tokens"])
+    # and the scale really is per slice: one slice's scale doubled moves only that layer's rows
+    w4b = dict(w4, ple_table=dict(w4["ple_table"], scales=w4["ple_table"]["scales"].copy()))
+    w4b["ple_table"]["scales"][:, 3] += np.uint16(0x80)  # bf16 exponent + 1: scale x 2
+    o1 = oracle.Oracle(cfg, w4, 1, 8, np.float64)
+    o2 = oracle.Oracle(cfg, w4b, 1, 8, np.float64)
+    t1 = oracle.table_rows(o1.ple_table, np.array([9]), np.float64).reshape(L, P)
+    t2 = oracle.table_rows(o2.ple_table, np.array([9]), np.float64).reshape(L, P)
+    np.testing.assert_array_equal(t2[3], 2 * t1[3])
+    np.testing.assert_array_equal(np.delete(t2, 3, 0), np.delete(t1, 3, 0))
+
+
+def test_int8_kv_cache_rows_on_the_grid_and_full_reforward(tiny):
+    """int8 K/V rows (One TPU chip, eight agents, Measured): every cached row lies on its own
+    255-level grid (codes times max|row| / 127), and cached decode still equals the full
+    re-forward that stores the same rows."""
+    cfg, w = tiny
+    pr = synth.make_prompts(cfg["vocab"], 1, 20, seed=5)
+    o = oracle.Oracle(cfg, w, max_batch=1, max_context=96, dtype=np.float64, kv_dtype="int8")
+    r = o.generate(pr, 10, keep_logits=True)
+    seq = np.concatenate([pr[0], r["tokens"][0, :-1]])
+    assert np.max(np.abs(o.forward_full(seq)[19:] - r["logits"][:, 0])) < 1e-9
+    n = len(seq)
+    for l in o.K:
+        for C in (o.K[l], o.Vc[l]):
+            rows = C[0, :n]
+            s = np.max(np.abs(rows), axis=-1, keepdims=True) / 127.0
+            c = rows / s
+            assert np.max(np.abs(c - np.rint(c))) < 1e-4 and np.max(np.abs(c)) <= 127 + 1e-4
+    # the bf16 cache is not on such a grid: the check tells the two apart
+    ob = oracle.Oracle(cfg, w, max_batch=1, max_context=96, dtype=np.float64)
+    ob.generate(pr, 2)
+    rows = ob.K[0][0, :20]
+    c = rows / (np.max(np.abs(rows), axis=-1, keepdims=True) / 127.0)
+    assert np.max(np.abs(c - np.rint(c))) > 1e-2
+
+
+def test_int8_kv_tracks_bf16_kv(tiny):
+    """Teacher-forced: int8 rows move the logits by far less than their spread (the pages
+    found int8 KV indistinguishable from bf16 in quality; this is only a sanity bound)."""
+    cfg, w = tiny
+    toks = synth.make_prompts(cfg["vocab"], 1, 24, seed=8)[0]
+    a = oracle.Oracle(cfg, w, 1, 32, np.float64)
+    b = oracle.Oracle(cfg, w, 1, 32, np.float64, kv_dtype="int8")
+    for p, t in enumerate(toks):
+        la = a.step([0], [t], [p])[0]
+        lb = b.step([0], [t], [p])[0]
+        cos = la @ lb / np.linalg.norm(la) / np.linalg.norm(lb)
+        assert cos > 0.999, (p, cos)
