@@ -13,7 +13,7 @@ DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("common.cuh", "gemv.cu
 DEPS.append(os.path.join(os.path.dirname(HERE), "include", "g4.h"))
 
 NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-              "-shared", "-Xcompiler", "-fPIC", "-diag-suppress", "177"]
+              "-shared", "-Xcompiler", "-fPIC"]
 
 
 def _nvcc():

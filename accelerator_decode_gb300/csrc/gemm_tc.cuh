@@ -55,8 +55,7 @@ __host__ __device__ inline size_t tc_stage_bytes(int bpad) {
   return 16384 /* raw weights (+scales) */ + 16384 /* A tile */ + (size_t)2 * bpad * 128 /* x parts */;
 }
 __host__ __device__ inline size_t tc_smem_bytes(int bpad) {
-  return 1024 /* alignment slack */ + kTcStages * tc_stage_bytes(bpad) + 256 /* barriers, flags */ +
-         4 * 64 * 4 /* GEGLU exchange */;
+  return 1024 /* alignment slack */ + kTcStages * tc_stage_bytes(bpad) + 256 /* barriers, flags */;
 }
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -130,7 +129,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3 * kTcStages + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kTcStages + 2);
   int* is_last_s = reinterpret_cast<int*>(bars + 3 * kTcStages + 3);
-  float* xch = reinterpret_cast<float*>(smem + kTcStages * stage_bytes + 256);  // [2][64] GEGLU exchange
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = blockIdx.x / a.ksplit, ks = blockIdx.x % a.ksplit;

@@ -429,7 +429,7 @@ __device__ __noinline__ bool mega_proj(const MegaArgs& a, const MegaPhase& ph, f
   constexpr int SGK = Fmt<FMT>::SGK, TK = Fmt<FMT>::TK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // descriptor fields in registers (the loops store to shared memory, where the descriptor lives)
-  const int in_mode = ph.in_mode, K = ph.K, r_parts = ph.r_parts, nR = ph.R, S_ = ph.S;
+  const int in_mode = ph.in_mode, K = ph.K, r_parts = ph.r_parts, nR = ph.R;
   const int spu = ph.spu, ksplit = ph.ksplit, n_units = ph.n_units, n_valid = ph.n_valid, epi = ph.epi;
   const float* x_in = ph.x_in;
   const int x_stride = ph.x_stride;
