@@ -72,11 +72,13 @@ def _owning(cfg):
     return [l < first or not any(full[j] == full[l] for j in range(first)) for l in range(L)]
 
 
-def algorithmic_bytes(cfg, fmt, batch, positions):
+def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False):
     """Unique bytes one decode step must move: every weight once (int4 at 0.5 B + a bf16 scale
     per 32, or bf16), the tied bf16 lm_head, and per sequence the visible K/V of the owning
     layers' caches (read once even when aliased), the new K/V row, the per-layer-embedding row
-    and the embedding row.  Returns (weight bytes, mean KV+row bytes per step over positions)."""
+    and the embedding row.  count_aliased also counts each KV-sharing layer's read of its
+    source cache (the bytes the attention kernels actually request).  Returns (weight bytes,
+    mean KV+row bytes per step over positions)."""
     H, P, V, L = cfg["hidden"], cfg["ple_dim"], cfg["vocab"], cfg["num_layers"]
     own = _owning(cfg)
     n_lin = L * P * H
@@ -93,12 +95,12 @@ def algorithmic_bytes(cfg, fmt, batch, positions):
         T = p + 1
         b = 0
         for l in range(L):
-            if not own[l]:
+            if not own[l] and not count_aliased:
                 continue
             full = synth.layer_is_full(cfg, l)
             d = cfg["head_dim_full"] if full else cfg["head_dim_sliding"]
             keys = T if full else min(T, cfg["sliding_window"])
-            b += keys * d * 2 * 2 + d * 2 * 2
+            b += keys * d * 2 * 2 + (d * 2 * 2 if own[l] else 0)
         b += L * P * 2 + H * 2
         kv.append(b * batch)
     return wbytes, float(np.mean(kv))
@@ -321,6 +323,7 @@ def run_gpu(args, wl, cfg, fmt):
 
     positions = [P0 + i for i in range(K)]
     wbytes, kvbytes = algorithmic_bytes(cfg, fmt, B, positions)
+    _, kv_aliased = algorithmic_bytes(cfg, fmt, B, positions, count_aliased=True)
     peak, peak_src = measured_peak()
     step_bytes = wbytes + kvbytes
     value = replica_throughput(world, B, K, ms_max)
@@ -364,7 +367,9 @@ def run_gpu(args, wl, cfg, fmt):
         "step_roofline": {"bytes_per_step": step_bytes, "weight_bytes": wbytes, "kv_and_rows_bytes": kvbytes,
                           "achieved": round(step_bytes / (ms_max / K / 1e3) / 1e9, 1), "peak": peak,
                           "frac": round(step_bytes / (ms_max / K / 1e3) / 1e9 / peak, 4), "unit": "GB/s",
-                          "peak_source": peak_src, "calibrated_copy_gbs": round(copy_gbs, 1)},
+                          "peak_source": peak_src, "calibrated_copy_gbs": round(copy_gbs, 1),
+                          "kv_and_rows_bytes_counting_aliased_reads": kv_aliased,
+                          "frac_counting_aliased_reads": round((wbytes + kv_aliased) / (ms_max / K / 1e3) / 1e9 / peak, 4)},
         "e2e": {"value": round(replica_throughput(world, B, K, e2e_s * 1e3), 2), "unit": "tok/s",
                 "h2d_bytes_per_step": 2 * 4 * B,
                 "d2h_bytes_per_step": 4 * B},

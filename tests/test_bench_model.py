@@ -45,3 +45,15 @@ def test_replay_schedule_grows_500_to_8000_in_20_turns():
     for i, (fresh, outs) in enumerate(sched[1:]):
         ctx += fresh + (1 if i > 0 else 0) + (outs - 1)
     assert ctx == 8639
+
+
+def test_aliased_variant_adds_the_sharing_layers_reads():
+    """Counting re-reads: the 20 KV-sharing layers (16 sliding reading layer 13, 4 full reading
+    layer 14) read their source's visible keys again, and write no K/V row."""
+    cfg = synth.get_config("e2b")
+    _, kv = bench.algorithmic_bytes(cfg, "w4a16", 1, [638])
+    _, kva = bench.algorithmic_bytes(cfg, "w4a16", 1, [638], count_aliased=True)
+    assert kva - kv == 16 * 512 * 1024 + 4 * 639 * 2048
+    _, kva2 = bench.algorithmic_bytes(cfg, "w4a16", 1, [99])
+    _, kva3 = bench.algorithmic_bytes(cfg, "w4a16", 1, [99], count_aliased=True)
+    assert kva3 - kva2 == 16 * 100 * 1024 + 4 * 100 * 2048
