@@ -173,11 +173,22 @@ int sgk(int fmt) { return fmt == G4_W4A16 ? Fmt<FMT_W4A16>::SGK : Fmt<FMT_BF16>:
 
 // Choose the per-CTA K chunk: enough CTAs to cover the SMs a few times, fewer, fatter CTAs
 // for very tall matrices.
+// Projections whose tiles take fewer bytes than this run with one K slice (no partial sums and
+// no last-CTA merge on their dependency chain); 0 (the default) splits every projection.
+// Environment G4_GEMV_UNSPLIT_BYTES, read once.
+size_t gemv_unsplit_bytes() {
+  static const size_t v = [] {
+    const char* e = getenv("G4_GEMV_UNSPLIT_BYTES");
+    return e ? (size_t)std::max(0LL, atoll(e)) : (size_t)0;
+  }();
+  return v;
+}
+
 void plan_lin(Lin& L, int sms, bool whole_k) {
   const int n_rg = L.n_rb / L.R;
   // start at one supergroup per CTA, halve the split while the grid exceeds 3 CTAs per SM; the
   // K slices are balanced (warps share a slice's tiles, whatever its supergroup count)
-  int ks = whole_k ? 1 : L.S;
+  int ks = (whole_k || L.bytes < gemv_unsplit_bytes()) ? 1 : L.S;
   while (ks > 1 && (long)n_rg * ks > 3L * sms) ks = cdiv(ks, 2);
   L.sg_per_cta = cdiv(L.S, ks);
   L.ksplit = cdiv(L.S, L.sg_per_cta);
