@@ -81,7 +81,8 @@ def dequant_w4a16(packed, scales, dtype=np.float32):
 
     packed: int32 [N, K/8]; element k in word k // 8, bits 4*(k % 8).., two's complement.
     scales: bf16 bits [N, K/G]; the group size G = K / scales.shape[1] is 32 for the linears
-    and the token embedding, 256 (one scale per layer slice) for the per-layer table.  The
+    and the token embedding, ple_dim (one scale per layer slice; 256 in E2B) for the
+    per-layer table.  The
     product q*s is exact (4-bit integer times an 8-bit significand); it is then rounded to
     bf16 as dequantising to bf16 does [P5, Two optimizations; P4, cell 1.2]."""
     packed = np.asarray(packed)
@@ -102,8 +103,9 @@ def dequant_w4a16(packed, scales, dtype=np.float32):
 
 def table_rows(table, rows, dtype=np.float32):
     """Rows of a vocabulary table (token embedding or per-layer table): bf16 bits [V, n], or
-    an int4 table {"packed", "scales"} dequantised row by row [P2, Step 3: the vocabulary
-    tables in int4 too; P5, Measured: the per-layer table quantised to int4]."""
+    an int4 table {"packed", "scales"} dequantised row by row [P2, What Changes and What
+    Stays, Step 3: int4 vocabulary tables and lm_head; P5, Measured: an int4 per-layer
+    table]."""
     if isinstance(table, dict):
         return dequant_w4a16(table["packed"][rows], table["scales"][rows], dtype)
     return bf16_bits_to_float(table[rows], dtype)
