@@ -427,8 +427,8 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
 template <int D, int HPC>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char asmem_k[];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   attn_unit<D, HPC>(a, blockIdx.x, blockIdx.y, blockIdx.z, asmem_k, 0, 1);
 }
 
@@ -437,8 +437,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 // may append its own key inside the attention launch).  One warp per row.
 template <int D>
 __global__ void __launch_bounds__(32) kv_write_kernel(const AttnArgs a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, lane = threadIdx.x;
   const int p = __ldcg(a.positions + b), slot = __ldcg(a.slots + b);
   if (p < 0 || p >= a.t_max || slot < 0 || slot >= a.max_batch) return;  // attention flags it

@@ -106,7 +106,12 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // Programmatic dependent launch.  Before pdl_wait() a kernel may only read data that no
 // kernel of the step writes (weights, RoPE tables); every global write and every read of an
-// activation comes after it.  Both are no-ops for a launch without the PDL attribute.
+// activation comes after it.  Kernels trigger their dependents only after their own wait, so
+// at most two kernels of the step are resident at once (the one computing and the next one
+// loading its weights): triggered at the start, every following kernel became resident in a
+// cascade, SMs ran out of room, and the CTA scheduler put two CTAs of one kernel on one SM
+// (half speed) while other SMs had none.  Both are no-ops for a launch without the PDL
+// attribute.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 

@@ -34,6 +34,7 @@
 #include "common.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
+#include "gemv_s.cuh"
 #include "mega.cuh"
 #include "misc.cuh"
 
@@ -54,6 +55,23 @@ bool cuda_ok(cudaError_t e, const char* what) {
   do {                                                     \
     if (!cuda_ok((call), #call)) return G4_ERR_CUDA;       \
   } while (0)
+
+// Makes `dev` current for the guard's lifetime and gives the caller's current device back
+// afterwards, so no entry point changes the calling thread's device.
+struct DeviceGuard {
+  int prev = -1, dev = -1;
+  cudaError_t err = cudaSuccess;
+  explicit DeviceGuard(int d) : dev(d) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) err = cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0 && prev != dev) cudaSetDevice(prev);
+  }
+};
+#define DEVICE_GUARD(d)   \
+  DeviceGuard dg_guard_(d); \
+  CK(dg_guard_.err)
 
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -285,6 +303,7 @@ struct Scratch {
   unsigned* cnt;
   float* am_val;
   int* am_idx;
+  int* err;
 };
 
 // Programmatic dependent launch for every kernel of the step (G4_PDL=0 disables it).
@@ -311,6 +330,15 @@ void launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStre
   cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Every kernel of a step prefers the largest shared-memory carve-out.  Under programmatic
+// dependent launch the next kernel's CTAs become resident while the current kernel runs and
+// stream their weights in; an SM configured for a smaller carve-out can take a CTA that needs
+// more shared memory only after it drains, which delays that CTA (and its weight loads) to
+// the end of the current kernel.  With one carve-out for all kernels any mix of CTAs fits.
+template <typename... KArgs>
+void carve_max(void (*k)(KArgs...)) {
+  cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+}
 // Opt every kernel into the full shared-memory carve-out once per process (never during a
 // stream capture).
 template <typename... KArgs>
@@ -318,12 +346,19 @@ void set_max_dyn(void (*k)(KArgs...), int optin) {
   cudaFuncAttributes fa{};
   if (cudaFuncGetAttributes(&fa, k) != cudaSuccess) return;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+  carve_max(k);
 }
 template <int FMT, int R, int EPI>
 void attrs_gemv(int optin) {
   set_max_dyn(gemv_kernel<FMT, R, 1, EPI>, optin);
   set_max_dyn(gemv_kernel<FMT, R, 2, EPI>, optin);
   set_max_dyn(gemv_kernel<FMT, R, 4, EPI>, optin);
+}
+template <int FMT, int R, int EPI>
+void attrs_staged(int optin) {
+  set_max_dyn(gemv_s_kernel<FMT, R, 1, EPI>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, R, 2, EPI>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, R, 4, EPI>, optin);
 }
 template <int D>
 void attrs_attn(int optin) {
@@ -344,6 +379,12 @@ int init_kernel_attrs(int device) {
   attrs_gemv<FMT_W4A16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_ARGMAX>(optin);
+  attrs_staged<FMT_W4A16, 1, EPI_STORE>(optin);
+  attrs_staged<FMT_BF16, 1, EPI_STORE>(optin);
+  attrs_staged<FMT_W4A16, 2, EPI_GEGLU>(optin);
+  attrs_staged<FMT_BF16, 2, EPI_GEGLU>(optin);
+  attrs_staged<FMT_W4A16, 1, EPI_PLE>(optin);
+  attrs_staged<FMT_BF16, 1, EPI_PLE>(optin);
   set_max_dyn(gemm_tc_kernel, optin);
   set_max_dyn(mega_step_kernel<1>, optin);
   set_max_dyn(mega_step_kernel<2>, optin);
@@ -352,6 +393,14 @@ int init_kernel_attrs(int device) {
   attrs_attn<128>(optin);
   attrs_attn<256>(optin);
   attrs_attn<512>(optin);
+  carve_max(embed_kernel);
+  carve_max(ple_combine_kernel);
+  carve_max(gather_rows_kernel);
+  carve_max(argmax_partials_kernel);
+  carve_max(kv_write_kernel<64>);
+  carve_max(kv_write_kernel<128>);
+  carve_max(kv_write_kernel<256>);
+  carve_max(kv_write_kernel<512>);
   cudaGetLastError();
   g_optin[device] = optin;
   return optin;
@@ -378,6 +427,148 @@ int gemv_grid(const Lin& L, int sms) {
   const int n_rg = L.n_rb / L.R;
   if (L.ksplit > 1) return n_rg * L.ksplit;
   return std::min(n_rg, 4 * sms);
+}
+
+// ------------------------------------------------------------------- staged GEMV launch
+// The staged projection (gemv_s.cuh) runs every 1-4-row projection but the lm_head; the
+// environment G4_GEMV_STAGED=0 sends them to the K-split GEMV instead (for comparisons).
+bool gemv_staged_on() {
+  static const bool on = [] {
+    const char* e = getenv("G4_GEMV_STAGED");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+constexpr int kSgSmemBudget = 110 * 1024;  // two CTAs of consecutive phases share an SM
+
+struct SPlan {
+  bool ok = false;
+  GemvSArgs a{};
+  size_t smem = 0;
+};
+
+// Partition of one projection over the SMs: clusters of C CTAs split K, clusters take row
+// groups round-robin.  Chooses C to minimise the tiles one CTA streams (rounds x R x slice),
+// counting 4 tiles per row group (its barrier and sums) and 16 for a cluster's final merge
+// (it overlaps the other ranks' last row group); ties go to the larger grid.  Then ring items
+// of up to 32 KB and as many ring slots as the shared-memory budget allows.
+SPlan plan_staged(const Lin& L, int NB, int pro, int norm_n, int sms) {
+  SPlan p;
+  const int n_rg = L.n_rb / L.R;
+  const bool w4 = L.fmt == G4_W4A16;
+  const int sgb = 8 * 512 + (w4 ? 512 : 0);
+  const int sg_k = sgk(L.fmt);
+  long best = -1;
+  for (int C = 1; C <= 8 && C <= L.S; ++C) {
+    const int spc = cdiv(L.S, C);
+    if (cdiv(L.S, spc) != C) continue;  // every rank gets a non-empty slice
+    int n_cl = std::min(n_rg, sms / C);
+    if (n_cl < 1) continue;
+    const int rounds = cdiv(n_rg, n_cl);
+    if (rounds > kSgMaxRounds) continue;
+    n_cl = cdiv(n_rg, rounds);
+    const long cost = (long)rounds * (L.R * spc * 8 + 4) + (C > 1 ? 16 : 0);
+    if (best < 0 || cost < best || (cost == best && n_cl * C > p.a.n_cl * p.a.C)) {
+      best = cost;
+      p.a.C = C;
+      p.a.n_cl = n_cl;
+      p.a.spc = spc;
+      p.a.rounds = rounds;
+    }
+  }
+  if (best < 0) return p;
+  GemvSArgs& a = p.a;
+  a.csg = std::max(1, std::min({a.spc, kSgMaxCsg, 32768 / (L.R * sgb)}));
+  a.slot_bytes = (L.R * a.csg * sgb + 127) / 128 * 128;
+  const int items = a.rounds * cdiv(a.spc, a.csg);
+  a.pro = pro;
+  a.norm_n = norm_n;
+  a.slots = std::min(kSgMaxSlots, items);
+  for (;;) {
+    const SgSmem m = sg_smem_plan(NB, L.R, sg_k, a);
+    p.smem = (size_t)m.total + 128;
+    if ((int)p.smem <= kSgSmemBudget || a.slots <= 2) break;
+    --a.slots;
+  }
+  p.ok = (int)p.smem <= kSgSmemBudget + 64 * 1024;
+  return p;
+}
+
+template <int FMT, int R, int EPI>
+void launch_staged_fmt(const GemvSArgs& a, int nb, size_t smem, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_cl * a.C);
+  cfg.blockDim = dim3(kSgThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (a.C > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = a.C;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (nb == 1) cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, R, 1, EPI>, a);
+  else if (nb == 2) cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, R, 2, EPI>, a);
+  else cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, R, 4, EPI>, a);
+}
+
+// y = W x through the staged kernel; false if the projection has no staged plan.
+bool run_staged(const Lin& L, int epi, const GemvIO& io, int n, float eps, int* err, int sms, cudaStream_t st) {
+  const int NB = n == 1 ? 1 : (n == 2 ? 2 : 4);
+  SPlan p = plan_staged(L, NB, io.pro, io.norm_n, sms);
+  if (!p.ok) return false;
+  GemvSArgs& a = p.a;
+  a.qw = L.qw;
+  a.sc = L.sc;
+  a.n_rb = L.n_rb;
+  a.S = L.S;
+  a.tiles = L.tiles;
+  a.K = L.K;
+  a.n_valid = L.n_valid;
+  a.nb = n;
+  a.x_in = io.x_in;
+  a.x_stride = io.x_stride;
+  a.r_in = io.r_in;
+  a.r_stride = io.r_stride;
+  a.g_r = io.g_r;
+  a.lambda = io.lambda;
+  a.g_a = io.g_a;
+  a.x_out = io.x_out;
+  a.eps = eps;
+  a.y = io.y;
+  a.y_stride = io.y_stride;
+  a.ple = io.ple;
+  a.ple_stride = io.ple_stride;
+  a.err = err;
+  const bool w4 = L.fmt == G4_W4A16;
+  switch (epi) {
+    case EPI_STORE:
+      if (w4) launch_staged_fmt<FMT_W4A16, 1, EPI_STORE>(a, n, p.smem, st);
+      else launch_staged_fmt<FMT_BF16, 1, EPI_STORE>(a, n, p.smem, st);
+      break;
+    case EPI_GEGLU:
+      if (w4) launch_staged_fmt<FMT_W4A16, 2, EPI_GEGLU>(a, n, p.smem, st);
+      else launch_staged_fmt<FMT_BF16, 2, EPI_GEGLU>(a, n, p.smem, st);
+      break;
+    case EPI_PLE:
+      if (w4) launch_staged_fmt<FMT_W4A16, 1, EPI_PLE>(a, n, p.smem, st);
+      else launch_staged_fmt<FMT_BF16, 1, EPI_PLE>(a, n, p.smem, st);
+      break;
+    default:
+      return false;
+  }
+  return true;
 }
 
 // Tensor-core path for batches >= G4_TC_MIN_BATCH (default 5; 0 disables it).  The GEMV
@@ -468,6 +659,7 @@ void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const S
     run_gemm(L, epi, io, n, eps, *tc, sms, st);
     return;
   }
+  if (n <= kMaxNB && epi != EPI_ARGMAX && gemv_staged_on() && run_staged(L, epi, io, n, eps, s.err, sms, st)) return;
   for (int b0 = 0; b0 < n; b0 += kMaxNB) {
     const int nb = std::min(kMaxNB, n - b0);
     GemvArgs a{};
@@ -601,7 +793,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
   const float eps = c.rms_eps;
-  Scratch s{h->gemv_part, h->gemv_cnt, h->am_val, h->am_idx};
+  Scratch s{h->gemv_part, h->gemv_cnt, h->am_val, h->am_idx, h->err};
   TcScratch tc{h->xt, h->tc_part, h->gemv_cnt, h->am_val, h->am_idx, h->err};
 
   EmbedArgs ea{d_tokens, d_idx, h->embed, h->ple_table, c.vocab, H, LP,
@@ -1410,7 +1602,7 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
 }
 
 void destroy(g4_handle* h) {
-  cudaSetDevice(h->device);
+  DeviceGuard dg(h->device);
   cudaDeviceSynchronize();
   for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second);
   for (void* p : h->allocs) cudaFree(p);
@@ -1445,7 +1637,7 @@ g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
   g4_status v = validate(cfg);
   if (v != G4_OK) return v;
   if (!weights) return G4_ERR_INVALID_ARG;
-  CK(cudaSetDevice(device));
+  DEVICE_GUARD(device);
   init_kernel_attrs(device);
   g4_handle* h = new g4_handle();
   h->cfg = *cfg;
@@ -1495,7 +1687,7 @@ g4_status g4_decode_step(g4_handle* h, g4_stream stream, int32_t n_seq, const in
                          const int32_t* d_tokens, const int32_t* d_positions, int32_t* d_next_ids, float* d_logits) {
   if (!h || !d_slots || !d_tokens || !d_positions || !d_next_ids) return G4_ERR_INVALID_ARG;
   if (n_seq < 1 || n_seq > h->cfg.max_batch) return G4_ERR_INVALID_ARG;
-  CK(cudaSetDevice(h->device));
+  DEVICE_GUARD(h->device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (st == nullptr) {  // the legacy default stream cannot be captured: launch directly
     return run_step(h, st, n_seq, d_slots, d_tokens, nullptr, d_positions, d_next_ids, d_logits);
@@ -1539,7 +1731,7 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
     if ((int64_t)start_pos[i] + len[i] > c.max_context) return G4_ERR_CONTEXT_OVERFLOW;
     order[i] = i;
   }
-  CK(cudaSetDevice(h->device));
+  DEVICE_GUARD(h->device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   auto upload = [&](const std::vector<int>& host) -> g4_status {
     if (h->pf_cap < host.size()) {
@@ -1647,7 +1839,7 @@ g4_status g4_profile_step(g4_handle* h, g4_stream stream, int32_t n_seq, const i
   if (!h || !d_slots || !d_tokens || !d_positions || !d_next_ids || !stats || !n_stats || repeats < 1)
     return G4_ERR_INVALID_ARG;
   if (n_seq < 1 || n_seq > h->cfg.max_batch) return G4_ERR_INVALID_ARG;
-  CK(cudaSetDevice(h->device));
+  DEVICE_GUARD(h->device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (h->mega_ok && h->mega_on && n_seq <= 2) {
     // persistent step: per-phase durations from the %globaltimer stamps CTA 0 takes after
@@ -1717,7 +1909,7 @@ g4_status g4_profile_step(g4_handle* h, g4_stream stream, int32_t n_seq, const i
 
 g4_status g4_get_device_error(g4_handle* h, g4_stream stream, int32_t* word_out) {
   if (!h) return G4_ERR_INVALID_ARG;
-  CK(cudaSetDevice(h->device));
+  DEVICE_GUARD(h->device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int w = 0;
   CK(cudaMemcpyAsync(&w, h->err, sizeof(int), cudaMemcpyDeviceToHost, st));
@@ -1740,7 +1932,7 @@ g4_status g4_linear_create(int device, int32_t weight_format, int32_t n_out, int
   if (weight_format != G4_BF16 && weight_format != G4_W4A16) return G4_ERR_INVALID_ARG;
   if (weight_format == G4_W4A16 && !d_scales) return G4_ERR_INVALID_ARG;
   *out = nullptr;
-  CK(cudaSetDevice(device));
+  DEVICE_GUARD(device);
   init_kernel_attrs(device);
   g4_linear_op* op = new g4_linear_op();
   op->h.device = device;
@@ -1777,14 +1969,14 @@ g4_status g4_linear_create(int device, int32_t weight_format, int32_t n_out, int
 
 g4_status g4_linear_forward(g4_linear_op* op, g4_stream stream, int32_t n_rows, const float* d_x, float* d_y) {
   if (!op || !d_x || !d_y || n_rows < 1 || n_rows > 64) return G4_ERR_INVALID_ARG;
-  CK(cudaSetDevice(op->h.device));
+  DEVICE_GUARD(op->h.device);
   GemvIO io;
   io.pro = PRO_PLAIN;
   io.x_in = d_x;
   io.x_stride = op->lin.K;
   io.y = d_y;
   io.y_stride = op->lin.n_valid;
-  Scratch s{op->h.gemv_part, op->h.gemv_cnt, nullptr, nullptr};
+  Scratch s{op->h.gemv_part, op->h.gemv_cnt, nullptr, nullptr, op->h.err};
   TcScratch tc{op->h.xt, op->h.tc_part, op->h.gemv_cnt, nullptr, nullptr, op->h.err};
   run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, op->h.sms, reinterpret_cast<cudaStream_t>(stream), &tc);
   CK(cudaGetLastError());
@@ -1793,7 +1985,7 @@ g4_status g4_linear_forward(g4_linear_op* op, g4_stream stream, int32_t n_rows, 
 
 void g4_linear_free(g4_linear_op* op) {
   if (!op) return;
-  cudaSetDevice(op->h.device);
+  DeviceGuard dg(op->h.device);
   cudaDeviceSynchronize();
   for (void* p : op->h.allocs) cudaFree(p);
   delete op;
@@ -1814,7 +2006,7 @@ std::map<int, ArgmaxScratch> g_am;
 g4_status g4_argmax_rows(int device, g4_stream stream, int32_t n_rows, int32_t n_cols, const float* d_logits,
                          int32_t* d_ids) {
   if (!d_logits || !d_ids || n_rows < 1 || n_rows > 64 || n_cols < 1) return G4_ERR_INVALID_ARG;
-  CK(cudaSetDevice(device));
+  DEVICE_GUARD(device);
   const int chunk = 4096;
   const int nchunk = cdiv(n_cols, chunk);
   const size_t need = (size_t)n_rows * nchunk;
@@ -1868,7 +2060,7 @@ g4_status g4_argmax_rows_static(int device, g4_stream stream, int32_t n_rows, in
     g_last_cuda = "g4_argmax_rows_static: at most 64 rows and 1,048,576 columns";
     return G4_ERR_INVALID_ARG;
   }
-  CK(cudaSetDevice(device));
+  DEVICE_GUARD(device);
   StaticArgmaxScratch* sc = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_static_mu);

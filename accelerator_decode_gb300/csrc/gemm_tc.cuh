@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
   const int nkb = kb1 - kb0;
   const int ncols = a.bpad <= 32 ? 32 : (a.bpad <= 64 ? 64 : 128);
 
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&full[s], 1);
@@ -459,13 +459,13 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const PrepArgs a) {
   __nv_bfloat16* gr_s = reinterpret_cast<__nv_bfloat16*>(rrow + a.kpad);
   __nv_bfloat16* ga_s = gr_s + a.kpad;
   const bool resid = a.pro == PRO_RESID, norm = a.pro != PRO_PLAIN && a.g_a != nullptr;
-  pdl_trigger();
   // gains are weights: staged before waiting for the previous kernel
   for (int c = tid; c < a.K / 8; c += nt) {
     if (resid) cp_async16(gr_s + 8 * c, a.g_r + 8 * c, true);
     if (norm) cp_async16(ga_s + 8 * c, a.g_a + 8 * c, true);
   }
   pdl_wait();
+  pdl_trigger();
   const float* x = a.x_in + (size_t)b * a.x_stride;
   for (int c = tid; c < a.kpad / 4; c += nt) {
     const bool ok = 4 * c < a.K;
@@ -517,8 +517,8 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const PrepArgs a) {
 __global__ void argmax_partials_kernel(const float* pv, const int* pi, int n_part, int* ids) {
   __shared__ float sv[32];
   __shared__ int si[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   float v = __int_as_float(0x7fc00000);
   int idx = 0x7fffffff;

@@ -263,7 +263,6 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
   const int nj = nT > warp ? (nT - warp + kGemvWarps - 1) / kGemvWarps : 0;  // tiles of this warp
   const int ng = (nj + kGrp - 1) / kGrp;
 
-  pdl_trigger();
   uint4 wb0[kGrp][R], wb1[kGrp][R];
   uint32_t sw0[kGrp][R], sw1[kGrp][R];
   auto load_grp = [&](uint4 (&wb)[kGrp][R], uint32_t (&sw)[kGrp][R], int rg_, int gi) {
@@ -285,6 +284,7 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
   int rg = blockIdx.x / a.ksplit;
   if (rg < n_rg && ng > 0) load_grp(wb0, sw0, rg, 0);  // weights never depend on activations
   pdl_wait();
+  pdl_trigger();
   gemv_prologue<NB>(a, smem, L, kc, k0, k1);
 
   float* xs = smem + L.xs;

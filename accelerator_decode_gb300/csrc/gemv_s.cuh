@@ -1,0 +1,559 @@
+// Staged weight-only projection for 1-4 activation rows: y[b, n] = sum_k W[n, k] x[b, k],
+// on the GEMV tile layout of gemv.cuh (lane = row, 16-byte tiles, supergroups of 8 tiles).
+//
+// A decode step is a chain of dependent projections, each too small to keep HBM busy on its
+// own, so the weights move ahead of the dependency: every CTA has a producer warp that
+// streams the CTA's share of the weight tiles into a shared-memory ring with bulk copies
+// (cp.async.bulk, mbarrier completion) from the moment the CTA is resident -- under
+// programmatic dependent launch that is while the previous kernel still runs -- and only the
+// eight compute warps wait for the previous kernel (griddepcontrol.wait) before staging the
+// activation rows with one wave of cp.async.  Norm gains are weights too: they are staged
+// before the wait.
+//
+// Work: CTAs form clusters of C; a cluster owns row groups rg = cluster, cluster + n_cl, ...
+// (R row blocks of 32 rows each), its rank-r CTA the K slice of supergroups
+// [r * spc, (r + 1) * spc).  No partial sum leaves the cluster: ranks 1..C-1 push the
+// 32 * R * NB sums of each row group into rank 0's shared memory with st.async (completing on
+// a per-row-group mbarrier) as soon as they have them, and go on with the next row group;
+// rank 0 adds them in rank order (deterministic) after its own last row group, then runs the
+// epilogues.  Dequantisation and accumulation are those of the GEMV (tile_fma): bf16(q * s)
+// weights, fp32 activations and sums.  Every wait is bounded; on expiry the CTA sets the
+// device error word, stops, and waits (bounded) for the copies it issued before it exits.
+#pragma once
+#include "common.cuh"
+#include "gemm_tc.cuh"
+#include "gemv.cuh"
+
+namespace g4 {
+
+constexpr int kSgWarps = 8;                      // compute warps
+constexpr int kSgThreads = (kSgWarps + 1) * 32;  // + the producer warp
+constexpr int kSgMaxSlots = 16;
+constexpr int kSgMaxRounds = 32;
+constexpr int kSgMaxCsg = 4;                     // supergroups per ring item and row block
+constexpr unsigned long long kSgTimeoutNs = 1000000000ull;  // 1 s
+
+struct GemvSArgs {
+  const uint4* qw;
+  const uint4* sc;
+  int n_rb, S, tiles, K, n_valid;
+  // partition (see the plan in g4.cu)
+  int C;           // cluster size = K slices
+  int n_cl;        // clusters (grid = n_cl * C)
+  int spc;         // supergroups per K slice
+  int csg;         // supergroups per ring item and row block (<= kSgMaxCsg)
+  int slots;       // ring slots
+  int slot_bytes;  // bytes per slot (multiple of 128)
+  int rounds;      // row groups per cluster (max)
+  int nb;          // activation rows (<= NB)
+  // prologue (as GemvArgs)
+  int pro;
+  const float* x_in;
+  int x_stride;
+  const float* r_in;
+  int r_stride;
+  const __nv_bfloat16* g_r;
+  float lambda;
+  const __nv_bfloat16* g_a;
+  float* x_out;
+  float eps;
+  int norm_n;
+  // epilogue
+  float* y;
+  int y_stride;
+  const float* ple;
+  int ple_stride;
+  int* err;
+};
+
+// Shared-memory plan (bytes from a 128-aligned base), identical on host and device.
+//   ring | barriers + flags | xs [NB][kc] | stage (x rows, r rows, two gain vectors) |
+//   red [rounds][warps][NV] | fin [rounds][NV] | norm scratch [32][4 NB] | xch [rounds][C-1][NV]
+struct SgSmem {
+  int bars, xs, stage, red, fin, nred, xch, total;
+};
+__host__ __device__ inline SgSmem sg_smem_plan(int NB, int R, int sgk, const GemvSArgs& a) {
+  SgSmem p;
+  const int nv = R * NB * 32;
+  int o = a.slots * a.slot_bytes;
+  p.bars = o;
+  o += (2 * a.slots + a.rounds) * 8 + 16;  // full, empty, per-row-group barriers; two flags
+  o = (o + 15) & ~15;
+  p.xs = o;
+  o += NB * a.spc * sgk * 4;
+  p.stage = o;
+  if (a.pro != PRO_PLAIN) o += (2 * NB * a.norm_n + a.norm_n) * 4;
+  p.red = o;
+  o += a.rounds * kSgWarps * nv * 4;
+  p.fin = o;
+  o += a.rounds * nv * 4;
+  p.nred = o;
+  o += 32 * 4 * NB * 4;
+  p.xch = o;
+  if (a.C > 1) o += a.rounds * (a.C - 1) * nv * 4;
+  p.total = o;
+  return p;
+}
+
+__device__ __forceinline__ unsigned long long sg_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t sg_su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ bool sg_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(sg_su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait.  With abort_s != nullptr it also gives up once another role aborted.
+__device__ __forceinline__ bool sg_wait(uint64_t* b, uint32_t parity, volatile int* abort_s) {
+  unsigned long long t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (sg_try(b, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (abort_s && *abort_s) return false;
+      const unsigned long long now = sg_now();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kSgTimeoutNs) return false;
+    }
+  }
+}
+__device__ __forceinline__ void sg_csync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kSgWarps * 32) : "memory"); }
+
+// Sums of M values over the 256 compute threads (one barrier); `red` holds 32 * M floats.
+template <int M>
+__device__ __forceinline__ void sg_sum(float (&v)[M], float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < M; ++i) v[i] = warp_sum(v[i]);
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < M; ++i) red[i * 32 + warp] = v[i];
+  }
+  sg_csync();
+#pragma unroll
+  for (int i = 0; i < M; ++i) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSgWarps; ++w) s += red[i * 32 + w];
+    v[i] = s;
+  }
+}
+
+// Gains of the prologue (weights: staged before the dependency wait).
+__device__ __forceinline__ void sg_stage_gains(const GemvSArgs& a, float* stage, int NB) {
+  if (a.pro == PRO_PLAIN) return;
+  const int n = a.norm_n;
+  __nv_bfloat16* gr = reinterpret_cast<__nv_bfloat16*>(stage + 2 * NB * n);
+  __nv_bfloat16* ga = gr + n;
+  for (int i = threadIdx.x; i < n / 8; i += kSgWarps * 32) {
+    if (a.pro == PRO_RESID) cp_async16(gr + 8 * i, a.g_r + 8 * i, true);
+    if (a.g_a) cp_async16(ga + 8 * i, a.g_a + 8 * i, true);
+  }
+}
+
+// Activation prologue on the compute warps (after the dependency wait): the K slice
+// [k0, k0 + kc) of NB rows into xs (zero beyond k1 and beyond nb).  PRO_NORM / PRO_RESID stage
+// whole rows first (one cp.async wave).  Every step here is latency: one pass takes all the
+// sums the norms need, one barrier adds them over the warps, one pass writes the slice (and,
+// in the grid's first CTA, the updated residual).  With x' = lambda (x + r g_r / d_r),
+// d_r = sqrt(mean r^2 + eps), the second norm's sum of squares is
+//   sum x'^2 = lambda^2 (sum x^2 + (2 / d_r) sum x r g_r + (1 / d_r^2) sum r^2 g_r^2),
+// so it needs no second pass.
+template <int NB>
+__device__ __forceinline__ void sg_prologue(const GemvSArgs& a, float* xs, float* stage, float* nred, int kc, int k0,
+                                            int k1) {
+  const int tid = threadIdx.x, nt = kSgWarps * 32;
+  if (a.pro == PRO_PLAIN) {
+    const int c4 = kc / 4;
+    for (int i = tid; i < NB * c4; i += nt) {
+      const int b = i / c4, c = i - b * c4, k = k0 + 4 * c;
+      const bool ok = b < a.nb && k < k1;
+      cp_async16(xs + b * kc + 4 * c, ok ? a.x_in + (size_t)b * a.x_stride + k : a.x_in, ok);
+    }
+    cp_async_wait_all();
+    sg_csync();
+    return;
+  }
+  const int n = a.norm_n;
+  float* xin = stage;
+  float* rin = xin + NB * n;
+  const __nv_bfloat16* gr = reinterpret_cast<const __nv_bfloat16*>(rin + NB * n);
+  const __nv_bfloat16* ga = gr + n;
+  const bool resid = a.pro == PRO_RESID;
+  const bool norm = a.g_a != nullptr;
+  const int c4 = n / 4;
+  for (int i = tid; i < NB * c4; i += nt) {
+    const int b = i / c4, c = i - b * c4;
+    const bool ok = b < a.nb;
+    cp_async16(xin + b * n + 4 * c, ok ? a.x_in + (size_t)b * a.x_stride + 4 * c : a.x_in, ok);
+    if (resid) cp_async16(rin + b * n + 4 * c, ok ? a.r_in + (size_t)b * a.r_stride + 4 * c : a.r_in, ok);
+  }
+  cp_async_wait_all();
+  sg_csync();
+  // per row: sum x^2, sum r^2, sum x r g_r, sum r^2 g_r^2
+  float t[4 * NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    float sx = 0.f, sr = 0.f, sxr = 0.f, srr = 0.f;
+    for (int k = tid; k < n; k += nt) {
+      const float x = xin[b * n + k];
+      sx += x * x;
+      if (resid) {
+        const float r = rin[b * n + k], rg = r * bf16f(gr[k]);
+        sr += r * r;
+        sxr += x * rg;
+        srr += rg * rg;
+      }
+    }
+    t[4 * b] = sx;
+    t[4 * b + 1] = sr;
+    t[4 * b + 2] = sxr;
+    t[4 * b + 3] = srr;
+  }
+  sg_sum<4 * NB>(t, nred);
+  float inv_r[NB], inv_a[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    inv_r[b] = resid ? 1.0f / rms_denom(t[4 * b + 1], n, a.eps) : 0.f;
+    float ss = t[4 * b];
+    if (resid) ss = a.lambda * a.lambda * (ss + 2.0f * inv_r[b] * t[4 * b + 2] + inv_r[b] * inv_r[b] * t[4 * b + 3]);
+    inv_a[b] = norm ? 1.0f / rms_denom(ss, n, a.eps) : 1.f;
+  }
+  const bool write_x = resid && blockIdx.x == 0;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (write_x && b < a.nb) {
+      for (int c = tid; c < c4; c += nt) {
+        float4 x = *reinterpret_cast<const float4*>(xin + b * n + 4 * c);
+        const float4 r = *reinterpret_cast<const float4*>(rin + b * n + 4 * c);
+        x.x = (x.x + r.x * inv_r[b] * bf16f(gr[4 * c])) * a.lambda;
+        x.y = (x.y + r.y * inv_r[b] * bf16f(gr[4 * c + 1])) * a.lambda;
+        x.z = (x.z + r.z * inv_r[b] * bf16f(gr[4 * c + 2])) * a.lambda;
+        x.w = (x.w + r.w * inv_r[b] * bf16f(gr[4 * c + 3])) * a.lambda;
+        *reinterpret_cast<float4*>(a.x_out + (size_t)b * a.x_stride + 4 * c) = x;
+      }
+    }
+    for (int k = k0 + tid; k < k0 + kc; k += nt) {
+      float v = 0.f;
+      if (b < a.nb && k < k1) {
+        v = xin[b * n + k];
+        if (resid) v = (v + rin[b * n + k] * inv_r[b] * bf16f(gr[k])) * a.lambda;
+        if (norm) v = v * inv_a[b] * bf16f(ga[k]);
+      }
+      xs[b * kc + (k - k0)] = v;
+    }
+  }
+  sg_csync();
+}
+
+// One tile position (TK values of k) of R row blocks against NB activation rows; the
+// activation values are read once for all R blocks.  Same arithmetic as tile_fma.
+template <int FMT, int NB, int R>
+__device__ __forceinline__ void tiles_fma(const uint4 (&wv)[R], const uint32_t (&s2)[R], const float* xs,
+                                          int xs_stride, float2 (&acc)[R][NB]) {
+  if constexpr (FMT == FMT_W4A16) {
+    const __nv_bfloat162 bias = __floats2bfloat162_rn(136.f, 136.f);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float4 xa[NB], xb[NB];
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        xa[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride + 8 * m);
+        xb[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride + 8 * m + 4);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint32_t w = m == 0 ? wv[r].x : m == 1 ? wv[r].y : m == 2 ? wv[r].z : wv[r].w;
+        const __nv_bfloat162 sc = as_bf162(s2[r]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t u = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+          const uint32_t p = as_u32(__hmul2(__hsub2(as_bf162(u), bias), sc));
+          const float2 wf = make_float2(bf16_lo(p), bf16_hi(p));
+#pragma unroll
+          for (int b = 0; b < NB; ++b) {
+            const float2 xv = j == 0 ? make_float2(xa[b].x, xa[b].y)
+                            : j == 1 ? make_float2(xa[b].z, xa[b].w)
+                            : j == 2 ? make_float2(xb[b].x, xb[b].y)
+                                     : make_float2(xb[b].z, xb[b].w);
+            acc[r][b] = __ffma2_rn(wf, xv, acc[r][b]);
+          }
+        }
+      }
+    }
+  } else {
+    float4 xa[NB], xb[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      xa[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride);
+      xb[b] = *reinterpret_cast<const float4*>(xs + b * xs_stride + 4);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const uint32_t w[4] = {wv[r].x, wv[r].y, wv[r].z, wv[r].w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float2 wf = make_float2(bf16_lo(w[m]), bf16_hi(w[m]));
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float2 xv = m == 0 ? make_float2(xa[b].x, xa[b].y)
+                          : m == 1 ? make_float2(xa[b].z, xa[b].w)
+                          : m == 2 ? make_float2(xb[b].x, xb[b].y)
+                                   : make_float2(xb[b].z, xb[b].w);
+          acc[r][b] = __ffma2_rn(wf, xv, acc[r][b]);
+        }
+      }
+    }
+  }
+}
+
+template <int FMT, int R, int NB, int EPI>
+__global__ void __launch_bounds__(kSgThreads, 2) gemv_s_kernel(const GemvSArgs a) {
+  using F = Fmt<FMT>;
+  constexpr bool W4 = FMT == FMT_W4A16;
+  constexpr int NV = R * NB * 32;
+  constexpr uint32_t kSgW = 8 * 512;           // weight bytes of one supergroup of one row block
+  constexpr uint32_t kSgS = W4 ? 512 : 0;      // its scale bytes
+  extern __shared__ __align__(128) uint8_t sg_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sg_raw) + 127) & ~uintptr_t(127));
+  const SgSmem L = sg_smem_plan(NB, R, F::SGK, a);
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + a.slots;
+  uint64_t* rbar = empty + a.slots;
+  volatile int* abort_s = reinterpret_cast<volatile int*>(rbar + a.rounds);  // tells the producer to stop
+  volatile int* cfail = abort_s + 1;  // compute warps: written before a barrier, read after it
+  float* xs = reinterpret_cast<float*>(smem + L.xs);
+  float* stage = reinterpret_cast<float*>(smem + L.stage);
+  float* red = reinterpret_cast<float*>(smem + L.red);   // [rounds][warps][NV]
+  float* fin = reinterpret_cast<float*>(smem + L.fin);   // [rounds][NV]
+  float* nred = reinterpret_cast<float*>(smem + L.nred);
+  float* xch = reinterpret_cast<float*>(smem + L.xch);   // [rounds][C-1][NV] (rank 0)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t rank = 0, cl = blockIdx.x;
+  if (a.C > 1) {
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(rank));
+    cl = blockIdx.x / a.C;
+  }
+  const int n_rg = a.n_rb / R;
+  const int sg0 = (int)rank * a.spc;
+  const int sg1 = min(a.S, sg0 + a.spc);
+  const int nsg = max(0, sg1 - sg0);
+  const int nch = (nsg + a.csg - 1) / a.csg;  // ring items per row group
+  const int units = (int)cl < n_rg ? (n_rg - 1 - (int)cl) / a.n_cl + 1 : 0;
+  const int n_items = units * nch;
+  const int kc = a.spc * F::SGK;
+  const int k0 = sg0 * F::SGK;
+  const int k1 = min(a.K, sg1 * F::SGK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.slots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSgWarps);
+    }
+    for (int r = 0; r < a.rounds; ++r) mbar_init(&rbar[r], 1);
+    *abort_s = 0;
+    *cfail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    // rank 0 expects the other ranks' sums of every row group it owns
+    if (a.C > 1 && rank == 0)
+      for (int u = 0; u < units; ++u) mbar_expect_tx(&rbar[u], (uint32_t)((a.C - 1) * NV * 4));
+  }
+  if (a.C > 1) {
+    // every rank's barriers are initialised before any rank pushes into them
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+  } else {
+    __syncthreads();
+  }
+
+  if (warp == kSgWarps) {
+    // ---------------- producer: weights only (no dependency on the previous kernel)
+    if (lane == 0) {
+      int issued = 0;
+      for (int it = 0; it < n_items; ++it) {
+        const int s = it % a.slots, ph = it / a.slots;
+        if (ph > 0 && !sg_wait(&empty[s], (ph - 1) & 1, abort_s)) {
+          if (!*abort_s) { set_err(a.err, G4_DEV_TIMEOUT); *abort_s = 1; }
+          break;
+        }
+        if (*abort_s) break;
+        const int u = it / nch, c = it - u * nch;
+        const int rg = (int)cl + u * a.n_cl;
+        const int cs0 = sg0 + c * a.csg;
+        const int ncs = min(sg1, cs0 + a.csg) - cs0;
+        uint8_t* dst = ring + (size_t)s * a.slot_bytes;
+        mbar_expect_tx(&full[s], (uint32_t)(R * ncs * (kSgW + kSgS)));
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const size_t rb = (size_t)rg * R + r;
+          bulk_g2s(dst + r * ncs * kSgW, a.qw + (rb * a.tiles + (size_t)cs0 * 8) * 32, ncs * kSgW, &full[s]);
+          if constexpr (W4)
+            bulk_g2s(dst + R * ncs * kSgW + r * ncs * kSgS, a.sc + (rb * a.S + cs0) * 32, ncs * kSgS, &full[s]);
+        }
+        ++issued;
+      }
+      // no copy may be in flight into this CTA's shared memory when it exits
+      for (int it = max(0, issued - a.slots); it < issued; ++it) sg_wait(&full[it % a.slots], (it / a.slots) & 1, nullptr);
+    }
+    return;
+  }
+
+  // ---------------- compute warps
+  if (units == 0) return;
+  sg_stage_gains(a, stage, NB);  // weights: before the dependency wait
+  pdl_wait();
+  pdl_trigger();
+  sg_prologue<NB>(a, xs, stage, nred, kc, k0, k1);
+  // A failed wait is recorded in cfail before the next barrier of the compute warps and acted
+  // on after it, so every warp leaves at the same point (no warp is left at a barrier).
+  bool ok = true;
+  for (int u = 0; u < units; ++u) {
+    float2 acc[R][NB];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+    for (int c = 0; c < nch && ok; ++c) {
+      const int it = u * nch + c, s = it % a.slots, ph = it / a.slots;
+      if (!sg_wait(&full[s], ph & 1, nullptr)) {
+        ok = false;
+        if (lane == 0) { set_err(a.err, G4_DEV_TIMEOUT); *cfail = 1; *abort_s = 1; }
+        break;
+      }
+      const int cs0 = sg0 + c * a.csg;
+      const int ncs = min(sg1, cs0 + a.csg) - cs0;
+      const uint8_t* src = ring + (size_t)s * a.slot_bytes;
+      // this warp's tiles of the item: tile warp of supergroup j of each row block (j < ncs);
+      // all loads first, then the arithmetic
+      uint4 wv[kSgMaxCsg][R];
+      uint32_t s2[kSgMaxCsg][R];
+#pragma unroll
+      for (int j = 0; j < kSgMaxCsg; ++j) {
+        if (j < ncs) {
+          const int i = warp + 8 * j;
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            wv[j][r] = *reinterpret_cast<const uint4*>(src + ((size_t)(r * ncs * 8 + i) * 32 + lane) * 16);
+            s2[j][r] = 0;
+            if constexpr (W4) {
+              const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + R * ncs * kSgW + (r * ncs + j) * kSgS +
+                                                                     lane * 16 + (warp >> 1) * 4);
+              const uint32_t hh = (warp & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+              s2[j][r] = hh | (hh << 16);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kSgMaxCsg; ++j) {
+        if (j < ncs) {
+          const float* xt = xs + (cs0 - sg0 + j) * F::SGK + warp * F::TK;
+          tiles_fma<FMT, NB, R>(wv[j], s2[j], xt, kc, acc);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // this warp's sums of row group u (its own slot: no barrier between row groups)
+    float* rb = red + (size_t)u * kSgWarps * NV;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) rb[warp * NV + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
+  }
+  sg_csync();
+  // threads add four values of a row group over the warps in warp order and keep (rank 0) or
+  // push (other ranks) them
+  for (int e = threadIdx.x; e < units * (NV / 4) && !*cfail; e += kSgWarps * 32) {
+    const int u = e / (NV / 4), q = e - u * (NV / 4);
+    const float* rb = red + (size_t)u * kSgWarps * NV;
+    {
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kSgWarps; ++w) {
+        const float4 v = reinterpret_cast<const float4*>(rb + w * NV)[q];
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
+      }
+      if (a.C > 1 && rank != 0) {
+        const uint32_t la = sg_su32(xch + ((size_t)(u * (a.C - 1) + rank - 1) * NV + 4 * q));
+        const uint32_t lb = sg_su32(&rbar[u]);
+        uint32_t ra, rbr;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(la), "r"(0));
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(rbr) : "r"(lb), "r"(0));
+        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
+                         ra),
+                     "f"(sum.x), "f"(sum.y), "f"(sum.z), "f"(sum.w), "r"(rbr)
+                     : "memory");
+      } else {
+        reinterpret_cast<float4*>(fin + u * NV)[q] = sum;
+      }
+    }
+  }
+  sg_csync();  // fin is read below by other threads
+  if (*cfail || (a.C > 1 && rank != 0)) {
+    if (*cfail && a.C > 1 && rank == 0 && threadIdx.x == 0) {
+      // other ranks may still push: leave only after every row group's pushes landed (bounded)
+      for (int u = 0; u < units; ++u) sg_wait(&rbar[u], 0, nullptr);
+    }
+    return;
+  }
+  if (a.C > 1 && threadIdx.x < NV / 4) {
+    // add the other ranks' sums in rank order
+    const int q = threadIdx.x;
+    for (int u = 0; u < units; ++u) {
+      if (!sg_wait(&rbar[u], 0, nullptr)) {
+        set_err(a.err, G4_DEV_TIMEOUT);
+        *cfail = 1;
+        break;
+      }
+      float4 sum = reinterpret_cast<const float4*>(fin + u * NV)[q];
+      for (int o = 0; o < a.C - 1; ++o) {
+        const float4 v = reinterpret_cast<const float4*>(xch + (size_t)(u * (a.C - 1) + o) * NV)[q];
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
+      }
+      reinterpret_cast<float4*>(fin + u * NV)[q] = sum;
+    }
+  }
+  sg_csync();
+  if (*cfail) {
+    if (threadIdx.x == 0)
+      for (int u = 0; u < units; ++u) sg_wait(&rbar[u], 0, nullptr);
+    return;
+  }
+  // epilogues: value v = (r * NB + b) * 32 + lane of row group u is output row
+  // (rg * R + r) * 32 + lane of batch row b
+  for (int e = threadIdx.x; e < units * NV; e += kSgWarps * 32) {
+    const int u = e / NV, v = e - u * NV;
+    const int ln = v & 31, rbk = v >> 5, b = rbk % NB, r = rbk / NB;
+    if (b >= a.nb) continue;
+    const int rg = (int)cl + u * a.n_cl;
+    const float* f = fin + u * NV;
+    if constexpr (EPI == EPI_GEGLU) {
+      if (r != 0) continue;
+      const int n = rg * 32 + ln;  // R == 2: block 0 = gate rows, block 1 = up rows
+      if (n < a.n_valid) a.y[(size_t)b * a.y_stride + n] = gelu_tanh(f[(0 * NB + b) * 32 + ln]) * f[(1 * NB + b) * 32 + ln];
+    } else {
+      const int n = (rg * R + r) * 32 + ln;
+      if (n >= a.n_valid) continue;
+      float val = f[v];
+      if constexpr (EPI == EPI_PLE) val = gelu_tanh(val) * a.ple[(size_t)b * a.ple_stride + n];
+      a.y[(size_t)b * a.y_stride + n] = val;
+    }
+  }
+}
+
+}  // namespace g4

@@ -21,8 +21,8 @@ struct EmbedArgs {
 
 // Grid (ceil((H + LP) / (8 * blockDim.x)), nb): each thread converts 8 bf16 (one 16-byte load).
 __global__ void embed_kernel(const EmbedArgs a) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y;
   int t = a.idx ? a.tokens[a.idx[b]] : a.tokens[b];
   if (t < 0 || t >= a.V) {
@@ -56,8 +56,8 @@ __global__ void embed_kernel(const EmbedArgs a) {
 __global__ void ple_combine_kernel(const float* pr, const float* tok, const __nv_bfloat16* g, int L, int P,
                                    float inv_sqrt_h, float inv_sqrt2, float eps, float* ple) {
   __shared__ float red[32];
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.y, l = blockIdx.x;
   const size_t base = ((size_t)b * L + l) * P;
   float ss[1] = {0.f};
@@ -77,8 +77,8 @@ __global__ void ple_combine_kernel(const float* pr, const float* tok, const __nv
 // strides in floats, multiples of 4).  dst and src must not overlap.
 __global__ void gather_rows_kernel(const float* src, int src_stride, float* dst, int dst_stride, const int* idx,
                                    int width) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int i = blockIdx.x;
   const float4* s4 = reinterpret_cast<const float4*>(src + (size_t)__ldcg(idx + i) * src_stride);
   float4* d4 = reinterpret_cast<float4*>(dst + (size_t)i * dst_stride);

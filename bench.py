@@ -106,8 +106,8 @@ def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False):
     return wbytes, float(np.mean(kv))
 
 
-# DRAM traffic / algorithmic bytes of a kernel, from one ncu capture of its current code
-# (profiles/gemv_w4a16_e2b_v8k_b1_full.md); traffic scales with the rows a launch streams.
+# DRAM traffic / algorithmic bytes of a kernel, from one ncu capture of its current code;
+# traffic scales with the rows a launch streams.
 # Keyed by (weight format, phase); a kernel changed since its capture has no entry.
 MEASURED_TRAFFIC_RATIO = {("w4a16", "gemv.gate_up"): 10716416 / 10616832}
 
@@ -221,7 +221,7 @@ def run_gpu(args, wl, cfg, fmt):
     K, W = args.steps, args.warmup
     max_ctx = ((P0 + max(K, W, n_out) + 1 + 63) // 64) * 64
     t_gen = time.perf_counter()
-    weights = synth.make_weights(cfg, fmt, seed=args.seed)
+    weights = synth.make_model_weights(cfg, fmt, seed=args.seed)
     prompts = synth.make_prompts(cfg["vocab"], B, P0, seed=args.seed, stream=rank)
     t_gen = time.perf_counter() - t_gen
     dec = Decoder(cfg, weights, max_batch=B, max_context=max_ctx, device=local)
@@ -451,7 +451,7 @@ def run_replay(args, wl, cfg, fmt):
                                   outputs=n_out)
     max_ctx = sched[0][0] + sum(a + o for a, o in sched[1:])
     max_ctx = ((max_ctx + 63) // 64) * 64
-    weights = synth.make_weights(cfg, fmt, seed=args.seed)
+    weights = synth.make_model_weights(cfg, fmt, seed=args.seed)
     dec = Decoder(cfg, weights, max_batch=B, max_context=max_ctx, device=local)
     dev = torch.device("cuda", local)
     st = torch.cuda.Stream()
@@ -524,7 +524,7 @@ def run_reference(args, wl, cfg, fmt):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
-    weights = synth.make_weights(cfg, fmt, seed=args.seed)
+    weights = synth.make_model_weights(cfg, fmt, seed=args.seed)
     B = wl["batch"]
     # bounded sample: the whole run (warm-up + steps) must end within a few minutes
     budget = args.ref_budget

@@ -31,7 +31,8 @@ What pins each part (tests/test_oracle_*.py):
                    the bf16 tables; the per-layer table's bytes against the printed weight
                    tree before and after its int4 quantisation
   rmsnorm          constant vectors, scale invariance, a hand-computed case
-  gelu_tanh        closed-form values and its distance to the erf GELU
+  gelu_tanh        closed-form values (z * sigmoid(2u) at hand-picked points, which an erf
+                   GELU or a dropped cubic term fails) and its distance to the erf GELU
   rope             identity at position 0, norm preservation, relative-position property
   visible_keys     brute-force dense masks for several windows
   attend           one key gives V_0; equal scores give the mean of V
@@ -42,8 +43,13 @@ What pins each part (tests/test_oracle_*.py):
   Oracle.step      cached decode against the full re-forward (forward_full); shared layers
                    move only when their source cache is perturbed; PLE with a zero projection
   Oracle (whole)   the constants the pages leave open (eps, RoPE theta, attention scale, norm
-                   placement, gain form, embedding scale) are parity unpinned beyond
-                   self-consistency: no trained weights or reference logits are available.
+                   placement, gain form) are parity unpinned beyond self-consistency: no
+                   trained weights or reference logits are available.
+  GeGLU order      parity unpinned (self-consistency only): the pages print the activation of
+                   the per-layer-input gate alone, so gelu on the MLP gate (not on up) is a
+                   reading.
+  embedding scale  parity unpinned (self-consistency only): x = E[t] * sqrt(H) parallels the
+                   printed sqrt(P) of the per-layer table; the pages do not print it.
 """
 import numpy as np
 

@@ -18,11 +18,11 @@ element k of row n lives in word k // 8 of the row, bits [4*(k % 8), 4*(k % 8) +
 two's-complement nibble (low nibble first).  Scales are bf16 [N, K // 32].
 """
 from .configs import CONFIGS, WORKLOADS, get_config, get_workload, layer_is_full, layer_mlp_width
-from .weights import make_weights, bf16_from_f32, linear_names, iter_linears
+from .weights import make_weights, make_model_weights, bf16_from_f32, linear_names, iter_linears, MODEL_DRAWS
 from .prompts import make_prompts, replay_schedule
 
 __all__ = [
     "CONFIGS", "WORKLOADS", "get_config", "get_workload", "layer_is_full", "layer_mlp_width",
-    "make_weights", "bf16_from_f32", "linear_names", "iter_linears", "make_prompts",
+    "make_weights", "make_model_weights", "MODEL_DRAWS", "bf16_from_f32", "linear_names", "iter_linears", "make_prompts",
     "replay_schedule",
 ]

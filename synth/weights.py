@@ -163,6 +163,23 @@ def make_weights(cfg, fmt, seed=0, std=0.02, scale_std=0.004, gain_std=0.0,
     return w
 
 
+# Draw parameters of each model as the workloads use it, beyond make_weights' defaults.  The
+# E2B-shaped models draw their q/k-norm gains at 0.5: with unit gains this random 35-layer
+# stack is chaotic after a few dozen tokens (attention scores reach |s| ~ 19 and the fp32
+# decoder drifts from its fp64 twin by 2.6e-2 in the logits at 24 tokens), so no fp32
+# implementation could be held to the logit tolerance; at 0.5 the scores shrink 4x and the
+# fp32 / fp64 difference stays near 1e-6.  The pages give no norm gains for this shape.
+MODEL_DRAWS = {"e2b": dict(qk_gain=0.5), "e2b-v8k": dict(qk_gain=0.5)}
+
+
+def make_model_weights(cfg, fmt, seed=0, **overrides):
+    """The weights a workload runs on: make_weights with the model's draw parameters
+    (MODEL_DRAWS), which both the benchmark and the parity tests use."""
+    kw = dict(MODEL_DRAWS.get(cfg["name"], {}))
+    kw.update(overrides)
+    return make_weights(cfg, fmt, seed=seed, **kw)
+
+
 def iter_linears(weights):
     """(name, linear) for every linear tensor of a weight dict, in a fixed order."""
     yield "ple_model_proj", weights["ple_model_proj"]

@@ -35,7 +35,7 @@ QK_GAIN = 0.5
 @pytest.mark.parametrize("fmt", ["w4a16", "bf16"])
 def test_e2b_short_decode(rt, fmt, mode):
     cfg = synth.get_config("e2b")
-    w = synth.make_weights(cfg, fmt, seed=0, qk_gain=QK_GAIN)
+    w = synth.make_model_weights(cfg, fmt, seed=0)
     prompts = synth.make_prompts(cfg["vocab"], 1, 24, seed=0)
     ref = oracle.Oracle(cfg, w, max_batch=1, max_context=64).generate(prompts, 8, keep_logits=True)
     dec = rt.Decoder(cfg, w, max_batch=1, max_context=64)
@@ -71,7 +71,7 @@ def test_e2b_batch64_sampled_sequences(rt):
     at E2B size.  Sequences are independent, so the oracle decodes a sample of them alone;
     every sampled sequence's logits must match, teacher-forced on the oracle's tokens."""
     cfg = synth.get_config("e2b")
-    w = synth.make_weights(cfg, "w4a16", seed=0, qk_gain=QK_GAIN)
+    w = synth.make_model_weights(cfg, "w4a16", seed=0)
     B, T, n_out = 64, 8, 3
     prompts = synth.make_prompts(cfg["vocab"], B, T, seed=3)
     sample = [0, 17, 42, 63]

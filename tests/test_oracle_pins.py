@@ -122,6 +122,27 @@ def test_gelu_tanh_identities():
     np.testing.assert_allclose(oracle.gelu_tanh(np.array([20.0, -20.0])), [20.0, 0.0], atol=1e-12)
 
 
+def test_gelu_tanh_against_logistic_closed_form():
+    """The tanh form of GELU ("Porting Gemma 4 E2B to SGLang-JAX", Step 3: gelu with
+    approximate=True) equals z * sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3), since
+    (1 + tanh u) / 2 = 1 / (1 + exp(-2u)).  Written with exp instead of tanh, the points below
+    pin the cubic term, its coefficient and the sqrt(2/pi) factor; the erf form of GELU differs
+    from it by more than 1e-4 at z = 1, so an erf GELU in the oracle fails here."""
+    def logistic_form(z):
+        u = math.sqrt(2.0 / math.pi) * (z + 0.044715 * z ** 3)
+        return z / (1.0 + math.exp(-2.0 * u))
+
+    points = [1.0, -0.5, 2.0, 0.25, -3.0]
+    got = oracle.gelu_tanh(np.array(points, np.float64))
+    for z, g in zip(points, got):
+        assert abs(g - logistic_form(z)) <= 1e-12, (z, g)
+    erf_gelu_1 = 0.5 * (1.0 + math.erf(1.0 / math.sqrt(2.0)))
+    assert abs(got[0] - erf_gelu_1) > 1e-4
+    # without the cubic term the value at z = 2 moves by ~2e-2
+    u_lin = math.sqrt(2.0 / math.pi) * 2.0
+    assert abs(got[2] - 2.0 / (1.0 + math.exp(-2.0 * u_lin))) > 1e-2
+
+
 # ------------------------------------------------------------------------------------- rope
 def test_rope_identity_norm_and_relative_position():
     d = 16
