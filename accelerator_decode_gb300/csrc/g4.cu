@@ -142,6 +142,12 @@ struct g4_handle {
   int* err = nullptr;
   // prefill staging
   int* pf_buf = nullptr;
+  // staged decode step (1-4 rows): row-group counters per staged launch of a step, and the
+  // raw K-slice partial sums each projection hands to the next kernel ([kSgMaxParts][4][width])
+  unsigned* sg_ctr = nullptr;
+  float *sq_qkv = nullptr, *sq_rattn = nullptr, *sq_gu = nullptr, *sq_rmlp = nullptr, *sq_pg = nullptr,
+        *sq_rple = nullptr, *sq_pr = nullptr;
+  int sq_qkv_w = 0, sq_gu_w = 0;
   size_t pf_cap = 0;
   int* step_next = nullptr;
   float* step_logits = nullptr;
@@ -284,6 +290,8 @@ struct GemvIO {
   int x_stride = 0;
   const float* r_in = nullptr;
   int r_stride = 0;
+  int r_parts = 1;
+  long r_part_stride = 0;
   const __nv_bfloat16* g_r = nullptr;
   float lambda = 1.f;
   const __nv_bfloat16* g_a = nullptr;
@@ -354,11 +362,11 @@ void attrs_gemv(int optin) {
   set_max_dyn(gemv_kernel<FMT, R, 2, EPI>, optin);
   set_max_dyn(gemv_kernel<FMT, R, 4, EPI>, optin);
 }
-template <int FMT, int R, int EPI>
+template <int FMT>
 void attrs_staged(int optin) {
-  set_max_dyn(gemv_s_kernel<FMT, R, 1, EPI>, optin);
-  set_max_dyn(gemv_s_kernel<FMT, R, 2, EPI>, optin);
-  set_max_dyn(gemv_s_kernel<FMT, R, 4, EPI>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, 1, 1, EPI_STORE>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, 1, 2, EPI_STORE>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, 1, 4, EPI_STORE>, optin);
 }
 template <int D>
 void attrs_attn(int optin) {
@@ -379,12 +387,8 @@ int init_kernel_attrs(int device) {
   attrs_gemv<FMT_W4A16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_ARGMAX>(optin);
-  attrs_staged<FMT_W4A16, 1, EPI_STORE>(optin);
-  attrs_staged<FMT_BF16, 1, EPI_STORE>(optin);
-  attrs_staged<FMT_W4A16, 2, EPI_GEGLU>(optin);
-  attrs_staged<FMT_BF16, 2, EPI_GEGLU>(optin);
-  attrs_staged<FMT_W4A16, 1, EPI_PLE>(optin);
-  attrs_staged<FMT_BF16, 1, EPI_PLE>(optin);
+  attrs_staged<FMT_W4A16>(optin);
+  attrs_staged<FMT_BF16>(optin);
   set_max_dyn(gemm_tc_kernel, optin);
   set_max_dyn(mega_step_kernel<1>, optin);
   set_max_dyn(mega_step_kernel<2>, optin);
@@ -430,8 +434,9 @@ int gemv_grid(const Lin& L, int sms) {
 }
 
 // ------------------------------------------------------------------- staged GEMV launch
-// The staged projection (gemv_s.cuh) runs every 1-4-row projection but the lm_head; the
-// environment G4_GEMV_STAGED=0 sends them to the K-split GEMV instead (for comparisons).
+// The staged projection (gemv_s.cuh) runs every projection of a decode step of 1-4 rows but
+// the lm_head; the environment G4_GEMV_STAGED=0 sends them to the K-split GEMV instead (for
+// comparisons).
 bool gemv_staged_on() {
   static const bool on = [] {
     const char* e = getenv("G4_GEMV_STAGED");
@@ -440,53 +445,55 @@ bool gemv_staged_on() {
   return on;
 }
 
-constexpr int kSgSmemBudget = 110 * 1024;  // two CTAs of consecutive phases share an SM
+constexpr int kSgSmemBudget = 110 * 1024;  // CTAs of two consecutive launches share an SM
+constexpr int kSgCtrSlots = 512;           // staged launches of one step (row-group counters)
 
+// Partition of one projection over the SMs: C K slices (C = 1 when the epilogue needs whole
+// sums), floor(sms / C) * C CTAs, row blocks taken one at a time.  Chooses C to minimise the
+// tiles the busiest CTA streams, ceil(row blocks / CTAs per slice) x slice, counting 4 tiles
+// per row block taken (its sums) and 8 per extra part the consumer adds; ties go to fewer
+// slices.  Then ring items of up to 32 KB and as many ring slots as the shared-memory budget
+// allows.
 struct SPlan {
   bool ok = false;
   GemvSArgs a{};
   size_t smem = 0;
+  int grid = 0;
 };
-
-// Partition of one projection over the SMs: clusters of C CTAs split K, clusters take row
-// groups round-robin.  Chooses C to minimise the tiles one CTA streams (rounds x R x slice),
-// counting 4 tiles per row group (its barrier and sums) and 16 for a cluster's final merge
-// (it overlaps the other ranks' last row group); ties go to the larger grid.  Then ring items
-// of up to 32 KB and as many ring slots as the shared-memory budget allows.
-SPlan plan_staged(const Lin& L, int NB, int pro, int norm_n, int sms) {
+SPlan plan_staged(const Lin& L, int NB, int pro, int norm_n, bool whole_sums, int sms) {
   SPlan p;
-  const int n_rg = L.n_rb / L.R;
   const bool w4 = L.fmt == G4_W4A16;
   const int sgb = 8 * 512 + (w4 ? 512 : 0);
   const int sg_k = sgk(L.fmt);
+  const int n_rb = L.n_rb;  // units: single row blocks (R = 1)
   long best = -1;
-  for (int C = 1; C <= 8 && C <= L.S; ++C) {
+  for (int C = 1; C <= kSgMaxParts && C <= L.S; ++C) {
+    if (whole_sums && C > 1) break;
     const int spc = cdiv(L.S, C);
-    if (cdiv(L.S, spc) != C) continue;  // every rank gets a non-empty slice
-    int n_cl = std::min(n_rg, sms / C);
-    if (n_cl < 1) continue;
-    const int rounds = cdiv(n_rg, n_cl);
-    if (rounds > kSgMaxRounds) continue;
-    n_cl = cdiv(n_rg, rounds);
-    const long cost = (long)rounds * (L.R * spc * 8 + 4) + (C > 1 ? 16 : 0);
-    if (best < 0 || cost < best || (cost == best && n_cl * C > p.a.n_cl * p.a.C)) {
+    if (cdiv(L.S, spc) != C) continue;  // every slice non-empty
+    const int per = sms / C;            // CTAs per slice
+    if (per < 1) break;
+    const int rounds = cdiv(n_rb, per);
+    const int cap = std::min(kSgMaxUnits, 2 * rounds + 1);
+    if ((long)cap * per < n_rb) continue;
+    const long cost = (long)rounds * (spc * 8 + 4) + 8L * (C - 1);
+    if (best < 0 || cost < best) {
       best = cost;
       p.a.C = C;
-      p.a.n_cl = n_cl;
       p.a.spc = spc;
-      p.a.rounds = rounds;
+      p.a.cap = cap;
+      p.grid = per * C;
     }
   }
   if (best < 0) return p;
   GemvSArgs& a = p.a;
-  a.csg = std::max(1, std::min({a.spc, kSgMaxCsg, 32768 / (L.R * sgb)}));
-  a.slot_bytes = (L.R * a.csg * sgb + 127) / 128 * 128;
-  const int items = a.rounds * cdiv(a.spc, a.csg);
+  a.csg = std::max(1, std::min({a.spc, kSgMaxCsg, 32768 / sgb}));
+  a.slot_bytes = (a.csg * sgb + 127) / 128 * 128;
   a.pro = pro;
   a.norm_n = norm_n;
-  a.slots = std::min(kSgMaxSlots, items);
+  a.slots = std::min(kSgMaxSlots, a.cap * cdiv(a.spc, a.csg) + 1);
   for (;;) {
-    const SgSmem m = sg_smem_plan(NB, L.R, sg_k, a);
+    const SgSmem m = sg_smem_plan(NB, 1, sg_k, a);
     p.smem = (size_t)m.total + 128;
     if ((int)p.smem <= kSgSmemBudget || a.slots <= 2) break;
     --a.slots;
@@ -495,38 +502,85 @@ SPlan plan_staged(const Lin& L, int NB, int pro, int norm_n, int sms) {
   return p;
 }
 
-template <int FMT, int R, int EPI>
-void launch_staged_fmt(const GemvSArgs& a, int nb, size_t smem, cudaStream_t st) {
+// One CTA per SM for every staged launch.  Consecutive launches share SMs (the next one streams
+// its weights while the current one computes), so each CTA takes a little under half of an SM;
+// with nothing else in the way, the CTA scheduler then puts two CTAs of ONE launch on an SM
+// wherever the previous launch left a hole, and such an SM runs both at half speed.  A wide
+// attention launch (more CTAs than SMs) made those holes, and they carried over from launch to
+// launch for the rest of the step.  The step therefore alternates two footprints:
+//   X: dynamic shared memory padded past half an SM (two X CTAs cannot share an SM);
+//   Y: padding warps that take the CTA's registers past half the register file (two Y CTAs
+//      cannot share one), with shared memory within the budget;
+// an X CTA and a Y CTA fit together (96 registers a thread by construction).
+constexpr int kSgSmemPerSm = 228 * 1024;     // shared memory of one SM
+constexpr int kSgSmemPerCta = 1024;          // reserved by the system per resident CTA
+constexpr int kSgXSmem = kSgSmemPerSm / 2 - kSgSmemPerCta + 2048;   // > half an SM with the reserve
+static_assert(2 * (kSgXSmem + kSgSmemPerCta) > kSgSmemPerSm, "X footprint must exceed half an SM");
+static_assert((kSgXSmem + kSgSmemPerCta) + (kSgSmemBudget + kSgSmemPerCta) <= kSgSmemPerSm,
+              "X and Y footprints must fit together");
+template <typename K>
+int staged_y_threads(K kernel) {
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || fa.numRegs <= 0) return kSgThreads;
+  const int r = (fa.numRegs + 7) / 8 * 8;           // allocation granularity
+  const int warps = std::max(kSgWarps + 2, 65536 / 2 / (32 * r) + 1);
+  // X (kSgThreads at r <= kSgMaxRegs) beside Y must still fit the register file
+  if (kSgThreads * kSgMaxRegs + warps * 32 * r > 65536) return kSgThreads;
+  return warps * 32;
+}
+template <int FMT, int NB>
+void launch_staged_nb(const GemvSArgs& a, int grid, size_t smem, int xy, cudaStream_t st) {
+  static const int y_threads = staged_y_threads(gemv_s_kernel<FMT, 1, NB, EPI_STORE>);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_cl * a.C);
-  cfg.blockDim = dim3(kSgThreads);
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(xy == 2 ? y_threads : kSgThreads);
+  if (xy == 1) smem = std::max(smem, (size_t)kSgXSmem);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  if (pdl_enabled()) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
-  if (a.C > 1) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = a.C;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = na;
-  if (nb == 1) cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, R, 1, EPI>, a);
-  else if (nb == 2) cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, R, 2, EPI>, a);
-  else cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, R, 4, EPI>, a);
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, 1, NB, EPI_STORE>, a);
 }
 
-// y = W x through the staged kernel; false if the projection has no staged plan.
-bool run_staged(const Lin& L, int epi, const GemvIO& io, int n, float eps, int* err, int sms, cudaStream_t st) {
+// Input of a staged projection (see gemv_s.cuh).  The residual branch and the PRO_GEGLU /
+// PRO_PLEG sources may come as `parts` K-slice partial sums, part q at base + q * part_stride.
+struct StagedIn {
+  int pro = PRO_PLAIN;
+  const float* x = nullptr;
+  int x_stride = 0;
+  int x_parts = 1;
+  long x_part_stride = 0;
+  const float* r = nullptr;
+  int r_stride = 0;
+  int r_parts = 1;
+  long r_part_stride = 0;
+  const __nv_bfloat16* g_r = nullptr;
+  float lambda = 1.f;
+  const __nv_bfloat16* g_a = nullptr;
+  float* x_out = nullptr;
+  const float* ple = nullptr;  // PRO_PLEG: multiplier rows
+  int ple_stride = 0;
+};
+// Output of a staged projection: raw sums, part c at y + c * part_stride.  `parts` receives C.
+struct StagedOut {
+  float* y = nullptr;
+  int y_stride = 0;
+  long part_stride = 0;
+  int* parts = nullptr;
+};
+
+// y = W x (raw K-slice partial sums; with whole_sums one slice, so y is the product) through
+// the staged kernel.  ctr: this launch's row-group counters ([2][kSgMaxParts], zero).  False if
+// the projection has no staged plan.
+// xy: 0 plain launch, 1 / 2 the X / Y footprint (above).
+bool run_staged(const Lin& L, const StagedIn& in, const StagedOut& out, int n, float eps, int* err, unsigned* ctr,
+                int sms, cudaStream_t st, bool whole_sums = false, int xy = 0) {
   const int NB = n == 1 ? 1 : (n == 2 ? 2 : 4);
-  SPlan p = plan_staged(L, NB, io.pro, io.norm_n, sms);
+  const int norm_n = (in.pro == PRO_NORM || in.pro == PRO_RESID) ? L.K : 0;
+  SPlan p = plan_staged(L, NB, in.pro, norm_n, whole_sums, sms);
   if (!p.ok) return false;
   GemvSArgs& a = p.a;
   a.qw = L.qw;
@@ -535,39 +589,35 @@ bool run_staged(const Lin& L, int epi, const GemvIO& io, int n, float eps, int* 
   a.S = L.S;
   a.tiles = L.tiles;
   a.K = L.K;
-  a.n_valid = L.n_valid;
+  a.n_valid = L.R == 2 ? 2 * L.n_valid : L.n_valid;  // raw rows: both halves of an interleaved pair
+  a.grab = ctr;
+  a.done = ctr + kSgMaxParts;
   a.nb = n;
-  a.x_in = io.x_in;
-  a.x_stride = io.x_stride;
-  a.r_in = io.r_in;
-  a.r_stride = io.r_stride;
-  a.g_r = io.g_r;
-  a.lambda = io.lambda;
-  a.g_a = io.g_a;
-  a.x_out = io.x_out;
+  a.x_in = in.x;
+  a.x_stride = in.x_stride;
+  a.x_parts = in.x_parts;
+  a.x_part_stride = in.x_part_stride;
+  a.r_in = in.r;
+  a.r_stride = in.r_stride;
+  a.r_parts = in.r_parts;
+  a.r_part_stride = in.r_part_stride;
+  a.g_r = in.g_r;
+  a.lambda = in.lambda;
+  a.g_a = in.g_a;
+  a.x_out = in.x_out;
   a.eps = eps;
-  a.y = io.y;
-  a.y_stride = io.y_stride;
-  a.ple = io.ple;
-  a.ple_stride = io.ple_stride;
+  a.y = out.y;
+  a.y_stride = out.y_stride;
+  a.y_part_stride = out.part_stride;
+  a.ple = in.ple;
+  a.ple_stride = in.ple_stride;
   a.err = err;
+  if (out.parts) *out.parts = a.C;
+  if ((int)p.smem > kSgSmemBudget) xy = 0;  // the footprints assume the budget
   const bool w4 = L.fmt == G4_W4A16;
-  switch (epi) {
-    case EPI_STORE:
-      if (w4) launch_staged_fmt<FMT_W4A16, 1, EPI_STORE>(a, n, p.smem, st);
-      else launch_staged_fmt<FMT_BF16, 1, EPI_STORE>(a, n, p.smem, st);
-      break;
-    case EPI_GEGLU:
-      if (w4) launch_staged_fmt<FMT_W4A16, 2, EPI_GEGLU>(a, n, p.smem, st);
-      else launch_staged_fmt<FMT_BF16, 2, EPI_GEGLU>(a, n, p.smem, st);
-      break;
-    case EPI_PLE:
-      if (w4) launch_staged_fmt<FMT_W4A16, 1, EPI_PLE>(a, n, p.smem, st);
-      else launch_staged_fmt<FMT_BF16, 1, EPI_PLE>(a, n, p.smem, st);
-      break;
-    default:
-      return false;
-  }
+  if (NB == 1) w4 ? launch_staged_nb<FMT_W4A16, 1>(a, p.grid, p.smem, xy, st) : launch_staged_nb<FMT_BF16, 1>(a, p.grid, p.smem, xy, st);
+  else if (NB == 2) w4 ? launch_staged_nb<FMT_W4A16, 2>(a, p.grid, p.smem, xy, st) : launch_staged_nb<FMT_BF16, 2>(a, p.grid, p.smem, xy, st);
+  else w4 ? launch_staged_nb<FMT_W4A16, 4>(a, p.grid, p.smem, xy, st) : launch_staged_nb<FMT_BF16, 4>(a, p.grid, p.smem, xy, st);
   return true;
 }
 
@@ -659,7 +709,6 @@ void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const S
     run_gemm(L, epi, io, n, eps, *tc, sms, st);
     return;
   }
-  if (n <= kMaxNB && epi != EPI_ARGMAX && gemv_staged_on() && run_staged(L, epi, io, n, eps, s.err, sms, st)) return;
   for (int b0 = 0; b0 < n; b0 += kMaxNB) {
     const int nb = std::min(kMaxNB, n - b0);
     GemvArgs a{};
@@ -678,6 +727,8 @@ void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const S
     a.x_stride = io.x_stride;
     a.r_in = io.r_in ? io.r_in + (size_t)b0 * io.r_stride : nullptr;
     a.r_stride = io.r_stride;
+    a.r_parts = io.r_parts;
+    a.r_part_stride = io.r_part_stride;
     a.g_r = io.g_r;
     a.lambda = io.lambda;
     a.g_a = io.g_a;
@@ -784,12 +835,230 @@ g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots
 // first layer after which no layer writes K/V on, only rows keep_idx[0 .. n_keep) (their
 // slots and positions in keep_slots / keep_pos) go on: a prompt row that ends no sequence
 // feeds nothing past its last K/V write.  n_keep == 0 ends the step there.
+// Attention launch of layer l (shared by both step paths).
+void launch_layer_attn(g4_handle* h, const Layer& Y, const float* qkv, int qkv_stride, int n, const int* d_slots,
+                       const int* d_pos, bool own, cudaStream_t st) {
+  const g4_config& c = h->cfg;
+  const Layer& Src = h->layers[Y.src];
+  AttnArgs a{};
+  a.qkv = qkv;
+  a.qkv_stride = qkv_stride;
+  a.nq = c.num_q_heads;
+  a.g_q = Y.q_norm;
+  a.g_k = Y.k_norm;
+  a.eps = c.rms_eps;
+  a.scale = Y.scale;
+  a.window = Y.full ? 0 : c.sliding_window;
+  a.own = own;
+  a.kc = h->kc[Src.kv];
+  a.vc = h->vc[Src.kv];
+  a.t_max = c.max_context;
+  a.max_batch = c.max_batch;
+  a.rope_cos = h->cos_t[Y.full];
+  a.rope_sin = h->sin_t[Y.full];
+  a.slots = d_slots;
+  a.positions = d_pos;
+  a.out = h->attn;
+  a.out_stride = c.num_q_heads * Y.d;
+  const int hpc = attn_hpc(c.num_q_heads, n);
+  const int max_keys = Y.full ? c.max_context : std::min(c.sliding_window, c.max_context);
+  a.nsplit = attn_nsplit(h->sms, c.num_q_heads, hpc, n, max_keys);
+  const long units = (long)n * (c.num_q_heads / hpc) * a.nsplit;
+  a.nstage = (cdiv(max_keys, a.nsplit) > kAttnTile && units <= h->sms) ? 2 : 1;
+  a.ws_ml = h->attn_ml;
+  a.ws_o = h->attn_o;
+  a.counters = h->attn_cnt;
+  a.err = h->err;
+  switch (Y.d) {
+    case 64: launch_attn_d<64>(a, hpc, n, st); break;
+    case 128: launch_attn_d<128>(a, hpc, n, st); break;
+    case 256: launch_attn_d<256>(a, hpc, n, st); break;
+    default: launch_attn_d<512>(a, hpc, n, st); break;
+  }
+}
+
+// Decode step of 1-4 rows on the staged projections (gemv_s.cuh).  Every projection but the
+// lm_head writes raw K-slice partial sums; the kernel that reads them adds the parts and applies
+// what the projection's epilogue would have: the GeGLU (down's input), the per-layer-input gate
+// (the per-layer projection's input), the residual update and norms (the next projection's
+// prologue), the q/k/v split (attention), the per-layer-embedding combine.
+g4_status run_step_staged(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens,
+                          const int* d_idx, const int* d_pos, int* d_next, float* d_logits, Prof* prof) {
+  const g4_config& c = h->cfg;
+  const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
+  const float eps = c.rms_eps;
+  const long ps_h = (long)kMaxNB * H;  // part strides of the [part][row][width] buffers
+  int seq = 0;                         // staged launches so far (their counter slots)
+  auto ctr = [&]() { return h->sg_ctr + (size_t)(seq++ % kSgCtrSlots) * 2 * kSgMaxParts; };
+  // whole: one K slice (attention reads q, k and v whole: its loads stay one round trip)
+  auto staged = [&](const Lin& Ln, const StagedIn& in, float* y, int y_stride, long part_stride, int* parts,
+                    const char* name, bool whole = false) -> g4_status {
+    ProfScope ps(prof, name, (double)Ln.bytes);
+    StagedOut out{y, y_stride, part_stride, parts};
+    const int xy = (seq & 1) ? 2 : 1;  // consecutive staged launches alternate footprints
+    if (!run_staged(Ln, in, out, n, eps, h->err, ctr(), h->sms, st, whole, xy)) return G4_ERR_UNSUPPORTED;
+    return G4_OK;
+  };
+
+  EmbedArgs ea{d_tokens, d_idx, h->embed, h->ple_table, c.vocab, H, LP,
+               (float)std::sqrt((double)H), (float)std::sqrt((double)P), h->x0, h->tok, h->err};
+  {
+    ProfScope ps(prof, "embed", (double)n * (H + LP) * 2);
+    launch(embed_kernel, dim3(cdiv(H + LP, 8 * 256), n), dim3(256), 0, st, ea);
+  }
+  int pr_parts = 1;
+  {
+    StagedIn in;
+    in.x = h->x0;
+    in.x_stride = H;
+    TRY(staged(h->pmp, in, h->sq_pr, LP, (long)kMaxNB * LP, &pr_parts, "gemv.ple_model_proj"));
+  }
+  {
+    ProfScope ps(prof, "ple_combine", 0.0);
+    launch(ple_combine_kernel, dim3(L, n), dim3(std::min(256, std::max(32, P))), 0, st, (const float*)h->sq_pr,
+           pr_parts, (long)kMaxNB * LP, (const float*)h->tok, h->g_ppn, L, P, (float)(1.0 / std::sqrt((double)H)),
+           (float)(1.0 / std::sqrt(2.0)), eps, h->ple);
+  }
+  float* cur = h->x0;
+  auto next_x = [&]() { return cur == h->xb[0] ? h->xb[1] : h->xb[0]; };
+  const int ts = h->trace_stride;
+  int rple_parts = 1;
+  for (int l = 0; l < L; ++l) {
+    const Layer& Y = h->layers[l];
+    const int nqd = c.num_q_heads * Y.d;
+    int qkv_parts = 1, o_parts = 1, gu_parts = 1, d_parts = 1, pg_parts = 1;
+    {  // QKV
+      StagedIn in;
+      in.x = cur;
+      in.x_stride = H;
+      in.g_a = Y.in_norm;
+      if (l == 0) {
+        in.pro = PRO_NORM;
+      } else {
+        const Layer& Pv = h->layers[l - 1];
+        in.pro = PRO_RESID;
+        in.r = h->sq_rple;
+        in.r_stride = H;
+        in.r_parts = rple_parts;
+        in.r_part_stride = ps_h;
+        in.g_r = Pv.post_ple_norm;
+        in.lambda = Pv.lambda;
+        in.x_out = next_x();
+      }
+      TRY(staged(Y.qkv, in, h->sq_qkv, h->sq_qkv_w, (long)kMaxNB * h->sq_qkv_w, &qkv_parts, "gemv.qkv", true));
+      if (l > 0) {
+        cur = in.x_out;
+        if (h->trace)
+          for (int i = 0; i < n; ++i)
+            cudaMemcpyAsync(h->trace + ((size_t)((l - 1) * 2 + 1) * c.max_batch + i) * ts, cur + (size_t)i * H,
+                            H * sizeof(float), cudaMemcpyDeviceToDevice, st);
+      }
+    }
+    {
+      ProfScope ps(prof, Y.full ? "attn.full" : "attn.sliding", 0.0);
+      if (qkv_parts != 1) return G4_ERR_UNSUPPORTED;   // attention reads whole q, k, v rows
+      launch_layer_attn(h, Y, h->sq_qkv, h->sq_qkv_w, n, d_slots, d_pos, Y.own != 0, st);
+      if (h->trace)
+        for (int i = 0; i < n; ++i)
+          cudaMemcpyAsync(h->trace + ((size_t)(l * 2) * c.max_batch + i) * ts, h->attn + (size_t)i * nqd,
+                          nqd * sizeof(float), cudaMemcpyDeviceToDevice, st);
+    }
+    {  // O
+      StagedIn in;
+      in.x = h->attn;
+      in.x_stride = nqd;
+      TRY(staged(Y.o, in, h->sq_rattn, H, ps_h, &o_parts, "gemv.o"));
+    }
+    {  // gate/up (raw rows: gate block j, up block j)
+      StagedIn in;
+      in.pro = PRO_RESID;
+      in.x = cur;
+      in.x_stride = H;
+      in.r = h->sq_rattn;
+      in.r_stride = H;
+      in.r_parts = o_parts;
+      in.r_part_stride = ps_h;
+      in.g_r = Y.post_attn_norm;
+      in.g_a = Y.pre_ffw_norm;
+      in.x_out = next_x();
+      TRY(staged(Y.gu, in, h->sq_gu, h->sq_gu_w, (long)kMaxNB * h->sq_gu_w, &gu_parts, "gemv.gate_up"));
+      cur = in.x_out;
+    }
+    {  // down: input gelu(gate) * up
+      StagedIn in;
+      in.pro = PRO_GEGLU;
+      in.x = h->sq_gu;
+      in.x_stride = h->sq_gu_w;
+      in.x_parts = gu_parts;
+      in.x_part_stride = (long)kMaxNB * h->sq_gu_w;
+      TRY(staged(Y.down, in, h->sq_rmlp, H, ps_h, &d_parts, "gemv.down"));
+    }
+    {  // per-layer-input gate (raw)
+      StagedIn in;
+      in.pro = PRO_RESID;
+      in.x = cur;
+      in.x_stride = H;
+      in.r = h->sq_rmlp;
+      in.r_stride = H;
+      in.r_parts = d_parts;
+      in.r_part_stride = ps_h;
+      in.g_r = Y.post_ffw_norm;
+      in.x_out = next_x();
+      TRY(staged(Y.pg, in, h->sq_pg, P, (long)kMaxNB * P, &pg_parts, "gemv.ple_gate"));
+      cur = in.x_out;
+    }
+    {  // per-layer projection: input gelu(gate) * ple_l
+      StagedIn in;
+      in.pro = PRO_PLEG;
+      in.x = h->sq_pg;
+      in.x_stride = P;
+      in.x_parts = pg_parts;
+      in.x_part_stride = (long)kMaxNB * P;
+      in.ple = h->ple + (size_t)l * P;
+      in.ple_stride = LP;
+      TRY(staged(Y.pp, in, h->sq_rple, H, ps_h, &rple_parts, "gemv.ple_proj"));
+    }
+  }
+  {  // final norm, lm_head, argmax (K-split GEMV; the branch comes in parts)
+    const Layer& Pv = h->layers[L - 1];
+    GemvIO io;
+    io.pro = PRO_RESID;
+    io.x_in = cur;
+    io.x_stride = H;
+    io.norm_n = H;
+    io.r_in = h->sq_rple;
+    io.r_stride = H;
+    io.r_parts = rple_parts;
+    io.r_part_stride = ps_h;
+    io.g_r = Pv.post_ple_norm;
+    io.lambda = Pv.lambda;
+    io.g_a = h->g_final;
+    io.x_out = next_x();
+    io.logits = d_logits;
+    io.logits_stride = c.vocab;
+    io.next_ids = d_next;
+    Scratch s{h->gemv_part, h->gemv_cnt, h->am_val, h->am_idx, h->err};
+    {
+      ProfScope ps(prof, "gemv.lm_head_argmax", (double)h->lm.bytes);
+      run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, h->sms, st, nullptr);
+    }
+    if (h->trace)
+      for (int i = 0; i < n; ++i)
+        cudaMemcpyAsync(h->trace + ((size_t)((L - 1) * 2 + 1) * c.max_batch + i) * ts, io.x_out + (size_t)i * H,
+                        H * sizeof(float), cudaMemcpyDeviceToDevice, st);
+  }
+  CK(cudaGetLastError());
+  return G4_OK;
+}
+
 g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, const int* d_tokens, const int* d_idx,
                    const int* d_pos, int* d_next, float* d_logits, Prof* prof = nullptr, bool kv_first = false,
                    const int* keep_idx = nullptr, const int* keep_slots = nullptr, const int* keep_pos = nullptr,
                    int n_keep = -1) {
   if (h->mega_ok && h->mega_on && n <= 2 && !prof && !kv_first)
     return run_step_mega(h, st, n, d_slots, d_tokens, d_idx, d_pos, d_next, d_logits, false);
+  if (gemv_staged_on() && n <= kMaxNB && !kv_first && n_keep < 0)
+    return run_step_staged(h, st, n, d_slots, d_tokens, d_idx, d_pos, d_next, d_logits, prof);
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, LP = L * P;
   const float eps = c.rms_eps;
@@ -814,7 +1083,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
   }
   {
     ProfScope ps(prof, "ple_combine", 0.0);
-    launch(ple_combine_kernel, dim3(L, n), dim3(std::min(256, std::max(32, P))), 0, st, (const float*)h->pr,
+    launch(ple_combine_kernel, dim3(L, n), dim3(std::min(256, std::max(32, P))), 0, st, (const float*)h->pr, 1, 0L,
            (const float*)h->tok, h->g_ppn, L, P, (float)(1.0 / std::sqrt((double)H)), (float)(1.0 / std::sqrt(2.0)),
            eps, h->ple);
   }
@@ -1537,6 +1806,21 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   TRY(dalloc(h, &h->r_mlp, (size_t)B * H));
   TRY(dalloc(h, &h->pg, (size_t)B * P));
   TRY(dalloc(h, &h->r_ple, (size_t)B * H));
+  {  // staged decode step buffers: kSgMaxParts parts of kMaxNB rows
+    h->sq_qkv_w = (nq + 2) * dmax;
+    h->sq_gu_w = 2 * Fmax;
+    const size_t R4 = (size_t)kSgMaxParts * kMaxNB;
+    TRY(dalloc(h, &h->sq_qkv, R4 * h->sq_qkv_w));
+    TRY(dalloc(h, &h->sq_rattn, R4 * H));
+    TRY(dalloc(h, &h->sq_gu, R4 * h->sq_gu_w));
+    TRY(dalloc(h, &h->sq_rmlp, R4 * H));
+    TRY(dalloc(h, &h->sq_pg, R4 * P));
+    TRY(dalloc(h, &h->sq_rple, R4 * H));
+    TRY(dalloc(h, &h->sq_pr, R4 * L * P));
+    const size_t nctr = (size_t)kSgCtrSlots * 2 * kSgMaxParts;
+    TRY(dalloc(h, &h->sg_ctr, nctr));
+    CK(cudaMemsetAsync(h->sg_ctr, 0, nctr * sizeof(unsigned), st));
+  }
   // GEMV scratch: partials of the widest split, one counter per row group (+1 for argmax)
   size_t part = 1, cnt = 1;
   auto acc_lin = [&](const Lin& Ln) {
@@ -1954,6 +2238,9 @@ g4_status g4_linear_create(int device, int32_t weight_format, int32_t n_out, int
     if (s == G4_OK) s = dalloc(&op->h, &op->h.xt, (size_t)tc_nkb(op->lin) * 2 * 64 * 128);
     if (s == G4_OK) s = dalloc(&op->h, &op->h.tc_part, (size_t)ks * 64 * (op->lin.n_rb / 4) * 128);
     if (s == G4_OK) s = dalloc(&op->h, &op->h.err, 1);
+    if (s == G4_OK) s = dalloc(&op->h, &op->h.sg_ctr, (size_t)2 * kSgMaxParts);
+    if (s == G4_OK && !cuda_ok(cudaMemsetAsync(op->h.sg_ctr, 0, 2 * kSgMaxParts * sizeof(unsigned), st), "memset"))
+      s = G4_ERR_CUDA;
     if (s == G4_OK && !cuda_ok(cudaMemsetAsync(op->h.err, 0, 4, st), "memset")) s = G4_ERR_CUDA;
   }
   cudaStreamSynchronize(st);
@@ -1978,7 +2265,18 @@ g4_status g4_linear_forward(g4_linear_op* op, g4_stream stream, int32_t n_rows, 
   io.y_stride = op->lin.n_valid;
   Scratch s{op->h.gemv_part, op->h.gemv_cnt, nullptr, nullptr, op->h.err};
   TcScratch tc{op->h.xt, op->h.tc_part, op->h.gemv_cnt, nullptr, nullptr, op->h.err};
-  run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, op->h.sms, reinterpret_cast<cudaStream_t>(stream), &tc);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n_rows <= kMaxNB && gemv_staged_on()) {  // the decode step's projection kernel, one K slice
+    StagedIn in;
+    in.x = d_x;
+    in.x_stride = op->lin.K;
+    StagedOut out{d_y, op->lin.n_valid, 0, nullptr};
+    if (run_staged(op->lin, in, out, n_rows, 0.f, op->h.err, op->h.sg_ctr, op->h.sms, st, true)) {
+      CK(cudaGetLastError());
+      return G4_OK;
+    }
+  }
+  run_gemv(op->lin, EPI_STORE, io, n_rows, 0.f, s, op->h.sms, st, &tc);
   CK(cudaGetLastError());
   return G4_OK;
 }

@@ -29,7 +29,7 @@
 namespace g4 {
 
 enum { FMT_BF16 = 0, FMT_W4A16 = 1 };
-enum { PRO_PLAIN = 0, PRO_NORM = 1, PRO_RESID = 2 };
+enum { PRO_PLAIN = 0, PRO_NORM = 1, PRO_RESID = 2, PRO_GEGLU = 3, PRO_PLEG = 4 };  // last two: staged GEMV only
 enum { EPI_STORE = 0, EPI_GEGLU = 1, EPI_PLE = 2, EPI_ARGMAX = 3 };
 
 constexpr int kGemvWarps = 4;
@@ -53,6 +53,8 @@ struct GemvArgs {
   int x_stride;
   const float* r_in;
   int r_stride;
+  int r_parts;        // > 1: r_in holds K-slice partial sums, part q at r_in + q * r_part_stride
+  long r_part_stride;
   const __nv_bfloat16* g_r;
   float lambda;
   const __nv_bfloat16* g_a;
@@ -179,11 +181,27 @@ __device__ __forceinline__ void gemv_prologue(const GemvArgs& a, float* smem, co
   __nv_bfloat16* ga = gr + n;
   const bool resid = a.pro == PRO_RESID;
   const int c4 = n / 4;
+  const bool r_split = resid && a.r_parts > 1;
   for (int i = tid; i < NB * c4; i += nt) {
     const int b = i / c4, c = i - b * c4;
     const bool ok = b < a.nb;
     cp_async16(xin + b * n + 4 * c, ok ? a.x_in + (size_t)b * a.x_stride + 4 * c : a.x_in, ok);
-    if (resid) cp_async16(rin + b * n + 4 * c, ok ? a.r_in + (size_t)b * a.r_stride + 4 * c : a.r_in, ok);
+    if (resid && !r_split) cp_async16(rin + b * n + 4 * c, ok ? a.r_in + (size_t)b * a.r_stride + 4 * c : a.r_in, ok);
+    if (r_split) {  // the branch's K-slice parts, added in part order
+      float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok) {
+        const float4* src = reinterpret_cast<const float4*>(a.r_in + (size_t)b * a.r_stride) + c;
+        r = __ldcg(src);
+        for (int q = 1; q < a.r_parts; ++q) {
+          const float4 v = __ldcg(src + q * a.r_part_stride / 4);
+          r.x += v.x;
+          r.y += v.y;
+          r.z += v.z;
+          r.w += v.w;
+        }
+      }
+      *reinterpret_cast<float4*>(rin + b * n + 4 * c) = r;
+    }
   }
   for (int i = tid; i < n / 8; i += nt) {
     if (resid) cp_async16(gr + 8 * i, a.g_r + 8 * i, true);

@@ -3,22 +3,25 @@
 //
 // A decode step is a chain of dependent projections, each too small to keep HBM busy on its
 // own, so the weights move ahead of the dependency: every CTA has a producer warp that
-// streams the CTA's share of the weight tiles into a shared-memory ring with bulk copies
-// (cp.async.bulk, mbarrier completion) from the moment the CTA is resident -- under
-// programmatic dependent launch that is while the previous kernel still runs -- and only the
-// eight compute warps wait for the previous kernel (griddepcontrol.wait) before staging the
-// activation rows with one wave of cp.async.  Norm gains are weights too: they are staged
-// before the wait.
+// streams its weight tiles into a shared-memory ring with bulk copies (cp.async.bulk,
+// mbarrier completion) from the moment the CTA is resident -- under programmatic dependent
+// launch that is while the previous kernel still computes -- and only the eight compute warps
+// wait for the previous kernel (griddepcontrol.wait) before staging the activation rows with
+// one wave of cp.async.  Norm gains are weights too: they are staged before the wait.
 //
-// Work: CTAs form clusters of C; a cluster owns row groups rg = cluster, cluster + n_cl, ...
-// (R row blocks of 32 rows each), its rank-r CTA the K slice of supergroups
-// [r * spc, (r + 1) * spc).  No partial sum leaves the cluster: ranks 1..C-1 push the
-// 32 * R * NB sums of each row group into rank 0's shared memory with st.async (completing on
-// a per-row-group mbarrier) as soon as they have them, and go on with the next row group;
-// rank 0 adds them in rank order (deterministic) after its own last row group, then runs the
-// epilogues.  Dequantisation and accumulation are those of the GEMV (tile_fma): bf16(q * s)
-// weights, fp32 activations and sums.  Every wait is bounded; on expiry the CTA sets the
-// device error word, stops, and waits (bounded) for the copies it issued before it exits.
+// Work.  K is cut into C slices of spc supergroups; CTA i owns slice i % C for the whole
+// launch, and its producer takes row groups (R row blocks of 32 rows) one at a time from a
+// counter of that slice (atomicAdd), as ring space frees.  A CTA that became resident late,
+// or shares its SM with another CTA of the same launch, simply takes fewer row groups, so the
+// split follows the speed each CTA actually gets.  The last CTA of a slice to finish taking
+// resets the slice's counters for the next launch.  No sum crosses CTAs: slice c writes its
+// raw partial sums to y + c * y_part_stride, and the kernel that reads them adds the C parts in
+// slice order (deterministic) as it stages them, together with what an epilogue would apply
+// (the GeGLU or per-layer-input gate of PRO_GEGLU / PRO_PLEG below, the residual update and
+// norms of PRO_RESID, the q/k/v split in attention).
+// Dequantisation and accumulation are those of the GEMV (tile_fma): bf16(q * s) weights,
+// fp32 activations and sums.  Every wait is bounded; on expiry the CTA sets the device error
+// word, stops, and waits (bounded) for the copies it issued before it exits.
 #pragma once
 #include "common.cuh"
 #include "gemm_tc.cuh"
@@ -29,8 +32,10 @@ namespace g4 {
 constexpr int kSgWarps = 8;                      // compute warps
 constexpr int kSgThreads = (kSgWarps + 1) * 32;  // + the producer warp
 constexpr int kSgMaxSlots = 16;
-constexpr int kSgMaxRounds = 32;
+constexpr int kSgMaxUnits = 32;                  // row groups one CTA may take
 constexpr int kSgMaxCsg = 4;                     // supergroups per ring item and row block
+constexpr int kSgMaxRegs = 96;                   // registers per thread (launch padding relies on it)
+constexpr int kSgMaxParts = 4;                   // K slices of one launch (and parts of an input)
 constexpr unsigned long long kSgTimeoutNs = 1000000000ull;  // 1 s
 
 struct GemvSArgs {
@@ -38,59 +43,66 @@ struct GemvSArgs {
   const uint4* sc;
   int n_rb, S, tiles, K, n_valid;
   // partition (see the plan in g4.cu)
-  int C;           // cluster size = K slices
-  int n_cl;        // clusters (grid = n_cl * C)
-  int spc;         // supergroups per K slice
+  int C;           // K slices; CTA i owns slice i % C
+  int spc;         // supergroups per slice
   int csg;         // supergroups per ring item and row block (<= kSgMaxCsg)
   int slots;       // ring slots
   int slot_bytes;  // bytes per slot (multiple of 128)
-  int rounds;      // row groups per cluster (max)
+  int cap;         // row groups one CTA may take (<= kSgMaxUnits)
+  unsigned* grab;  // [C] row-group counters; zero before the launch, left zero after it
+  unsigned* done;  // [C] CTAs of the slice that stopped taking
   int nb;          // activation rows (<= NB)
-  // prologue (as GemvArgs)
+  // prologue (as GemvArgs, plus PRO_GEGLU / PRO_PLEG); the residual branch r and the
+  // PRO_GEGLU / PRO_PLEG sources may come as K-slice parts to be added in part order
   int pro;
   const float* x_in;
   int x_stride;
+  int x_parts;
+  long x_part_stride;
   const float* r_in;
   int r_stride;
+  int r_parts;
+  long r_part_stride;
   const __nv_bfloat16* g_r;
   float lambda;
   const __nv_bfloat16* g_a;
   float* x_out;
   float eps;
   int norm_n;
-  // epilogue
+  // output: slice c of row n of batch row b at y[c * y_part_stride + b * y_stride + n]
   float* y;
   int y_stride;
-  const float* ple;
+  long y_part_stride;
+  const float* ple;  // PRO_PLEG: multipliers [nb][ple_stride]
   int ple_stride;
   int* err;
 };
 
 // Shared-memory plan (bytes from a 128-aligned base), identical on host and device.
-//   ring | barriers + flags | xs [NB][kc] | stage (x rows, r rows, two gain vectors) |
-//   red [rounds][warps][NV] | fin [rounds][NV] | norm scratch [32][4 NB] | xch [rounds][C-1][NV]
+//   ring | barriers, slot tags, unit rows, flags | xs [NB][kc] |
+//   stage (x rows, r rows, two gain vectors) | red [cap][warps][NV] | norm scratch [32][4 NB]
 struct SgSmem {
-  int bars, xs, stage, red, fin, nred, xch, total;
+  int bars, tags, units, xs, stage, red, nred, total;
 };
 __host__ __device__ inline SgSmem sg_smem_plan(int NB, int R, int sgk, const GemvSArgs& a) {
   SgSmem p;
   const int nv = R * NB * 32;
   int o = a.slots * a.slot_bytes;
   p.bars = o;
-  o += (2 * a.slots + a.rounds) * 8 + 16;  // full, empty, per-row-group barriers; two flags
+  o += (2 * a.slots + 1) * 8;  // full, empty, done
+  p.tags = o;
+  o += a.slots * 4;            // unit of each slot's item (-1: no more)
+  p.units = o;
+  o += kSgMaxUnits * 4 + 16;   // row group of each unit; abort and fail flags
   o = (o + 15) & ~15;
   p.xs = o;
   o += NB * a.spc * sgk * 4;
   p.stage = o;
   if (a.pro != PRO_PLAIN) o += (2 * NB * a.norm_n + a.norm_n) * 4;
   p.red = o;
-  o += a.rounds * kSgWarps * nv * 4;
-  p.fin = o;
-  o += a.rounds * nv * 4;
+  o += a.cap * kSgWarps * nv * 4;
   p.nred = o;
   o += 32 * 4 * NB * 4;
-  p.xch = o;
-  if (a.C > 1) o += a.rounds * (a.C - 1) * nv * 4;
   p.total = o;
   return p;
 }
@@ -157,18 +169,76 @@ __device__ __forceinline__ void sg_stage_gains(const GemvSArgs& a, float* stage,
   }
 }
 
+// Inputs that are a function of another projection's raw sums, over the K slice [k0, k1):
+//   PRO_GEGLU: x[f] = gelu_tanh(g[f]) u[f], with g and u the gate and up rows of a tiled
+//              [gate block j | up block j] matrix (row of gate f: 64 (f / 32) + f % 32, up: +32);
+//   PRO_PLEG:  x[p] = gelu_tanh(g[p]) ple[p].
+// All parts' loads are in flight together; they are added in part order.
+template <int NB>
+__device__ __forceinline__ void sg_gated_input(const GemvSArgs& a, float* xs, int kc, int k0, int k1) {
+  const int tid = threadIdx.x, nt = kSgWarps * 32;
+  const int c4 = kc / 4;
+  const bool geglu = a.pro == PRO_GEGLU;
+  // two chunks of four values per thread and pass: all their loads first
+  for (int i0 = tid; i0 < NB * c4; i0 += 2 * nt) {
+    float4 g[2][kSgMaxParts], u[2][kSgMaxParts], m[2];
+    bool ok[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = i0 + h * nt, b = i / c4, c = i - b * c4, f = k0 + 4 * c;
+      ok[h] = i < NB * c4 && b < a.nb && f < k1;
+      if (!ok[h]) continue;
+      const size_t rg_ = geglu ? (size_t)((f >> 5) << 6) + (f & 31) : (size_t)f;
+      const float* base = a.x_in + (size_t)b * a.x_stride + rg_;
+#pragma unroll
+      for (int q = 0; q < kSgMaxParts; ++q) {
+        if (q < a.x_parts) {
+          g[h][q] = __ldcg(reinterpret_cast<const float4*>(base + q * a.x_part_stride));
+          if (geglu) u[h][q] = __ldcg(reinterpret_cast<const float4*>(base + q * a.x_part_stride + 32));
+        }
+      }
+      if (!geglu) m[h] = __ldcg(reinterpret_cast<const float4*>(a.ple + (size_t)b * a.ple_stride + f));
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = i0 + h * nt, b = i / c4, c = i - b * c4;
+      if (i >= NB * c4) continue;
+      float4 out = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok[h]) {
+        float4 gs = g[h][0], us = geglu ? u[h][0] : m[h];
+#pragma unroll
+        for (int q = 1; q < kSgMaxParts; ++q) {
+          if (q < a.x_parts) {
+            gs.x += g[h][q].x; gs.y += g[h][q].y; gs.z += g[h][q].z; gs.w += g[h][q].w;
+            if (geglu) { us.x += u[h][q].x; us.y += u[h][q].y; us.z += u[h][q].z; us.w += u[h][q].w; }
+          }
+        }
+        out = make_float4(gelu_tanh(gs.x) * us.x, gelu_tanh(gs.y) * us.y, gelu_tanh(gs.z) * us.z,
+                          gelu_tanh(gs.w) * us.w);
+      }
+      *reinterpret_cast<float4*>(xs + b * kc + 4 * c) = out;
+    }
+  }
+  sg_csync();
+}
+
 // Activation prologue on the compute warps (after the dependency wait): the K slice
 // [k0, k0 + kc) of NB rows into xs (zero beyond k1 and beyond nb).  PRO_NORM / PRO_RESID stage
-// whole rows first (one cp.async wave).  Every step here is latency: one pass takes all the
-// sums the norms need, one barrier adds them over the warps, one pass writes the slice (and,
-// in the grid's first CTA, the updated residual).  With x' = lambda (x + r g_r / d_r),
-// d_r = sqrt(mean r^2 + eps), the second norm's sum of squares is
+// whole rows first (one cp.async wave; the residual branch's parts land side by side in the
+// x-row area and are added in part order), then one pass takes all the sums the norms need,
+// one barrier adds them over the warps, and one pass writes the slice (and, in the grid's
+// first CTA, the updated residual).  With x' = lambda (x + r g_r / d_r), d_r = sqrt(mean r^2 +
+// eps), the second norm's sum of squares is
 //   sum x'^2 = lambda^2 (sum x^2 + (2 / d_r) sum x r g_r + (1 / d_r^2) sum r^2 g_r^2),
 // so it needs no second pass.
 template <int NB>
 __device__ __forceinline__ void sg_prologue(const GemvSArgs& a, float* xs, float* stage, float* nred, int kc, int k0,
                                             int k1) {
   const int tid = threadIdx.x, nt = kSgWarps * 32;
+  if (a.pro == PRO_GEGLU || a.pro == PRO_PLEG) {
+    sg_gated_input<NB>(a, xs, kc, k0, k1);
+    return;
+  }
   if (a.pro == PRO_PLAIN) {
     const int c4 = kc / 4;
     for (int i = tid; i < NB * c4; i += nt) {
@@ -188,11 +258,46 @@ __device__ __forceinline__ void sg_prologue(const GemvSArgs& a, float* xs, float
   const bool resid = a.pro == PRO_RESID;
   const bool norm = a.g_a != nullptr;
   const int c4 = n / 4;
+  const int parts = resid ? a.r_parts : 0;
   for (int i = tid; i < NB * c4; i += nt) {
     const int b = i / c4, c = i - b * c4;
     const bool ok = b < a.nb;
     cp_async16(xin + b * n + 4 * c, ok ? a.x_in + (size_t)b * a.x_stride + 4 * c : a.x_in, ok);
-    if (resid) cp_async16(rin + b * n + 4 * c, ok ? a.r_in + (size_t)b * a.r_stride + 4 * c : a.r_in, ok);
+    if (parts == 1) cp_async16(rin + b * n + 4 * c, ok ? a.r_in + (size_t)b * a.r_stride + 4 * c : a.r_in, ok);
+  }
+  if (parts > 1) {
+    // r in slices: two chunks per thread and pass, every part's loads in flight at once, added
+    // in part order
+    for (int i0 = tid; i0 < NB * c4; i0 += 2 * nt) {
+      float4 v[2][kSgMaxParts];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = i0 + h * nt, b = i / c4, c = i - b * c4;
+#pragma unroll
+        for (int q = 0; q < kSgMaxParts; ++q)
+          if (i < NB * c4 && q < parts && b < a.nb)
+            v[h][q] = __ldcg(reinterpret_cast<const float4*>(a.r_in + q * a.r_part_stride + (size_t)b * a.r_stride) + c);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = i0 + h * nt, b = i / c4, c = i - b * c4;
+        if (i >= NB * c4) continue;
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (b < a.nb) {
+          r = v[h][0];
+#pragma unroll
+          for (int q = 1; q < kSgMaxParts; ++q) {
+            if (q < parts) {
+              r.x += v[h][q].x;
+              r.y += v[h][q].y;
+              r.z += v[h][q].z;
+              r.w += v[h][q].w;
+            }
+          }
+        }
+        *reinterpret_cast<float4*>(rin + b * n + 4 * c) = r;
+      }
+    }
   }
   cp_async_wait_all();
   sg_csync();
@@ -313,8 +418,10 @@ __device__ __forceinline__ void tiles_fma(const uint4 (&wv)[R], const uint32_t (
   }
 }
 
+// Launched with kSgThreads threads, or with more (padding warps that only hold registers until
+// the CTA ends: see the launch code); registers capped so that the padding arithmetic holds.
 template <int FMT, int R, int NB, int EPI>
-__global__ void __launch_bounds__(kSgThreads, 2) gemv_s_kernel(const GemvSArgs a) {
+__global__ void __maxnreg__(kSgMaxRegs) gemv_s_kernel(const GemvSArgs a) {
   using F = Fmt<FMT>;
   constexpr bool W4 = FMT == FMT_W4A16;
   constexpr int NV = R * NB * 32;
@@ -326,29 +433,22 @@ __global__ void __launch_bounds__(kSgThreads, 2) gemv_s_kernel(const GemvSArgs a
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + a.slots;
-  uint64_t* rbar = empty + a.slots;
-  volatile int* abort_s = reinterpret_cast<volatile int*>(rbar + a.rounds);  // tells the producer to stop
-  volatile int* cfail = abort_s + 1;  // compute warps: written before a barrier, read after it
+  uint64_t* done = empty + a.slots;               // the compute warps have finished (producer drain)
+  volatile int* tag = reinterpret_cast<volatile int*>(smem + L.tags);     // [slots] unit of the item
+  volatile int* unit_rg = reinterpret_cast<volatile int*>(smem + L.units);  // [kSgMaxUnits]
+  volatile int* abort_s = unit_rg + kSgMaxUnits;  // tells the producer to stop
+  volatile int* cfail = abort_s + 1;              // compute warps: written before a barrier, read after it
   float* xs = reinterpret_cast<float*>(smem + L.xs);
   float* stage = reinterpret_cast<float*>(smem + L.stage);
-  float* red = reinterpret_cast<float*>(smem + L.red);   // [rounds][warps][NV]
-  float* fin = reinterpret_cast<float*>(smem + L.fin);   // [rounds][NV]
+  float* red = reinterpret_cast<float*>(smem + L.red);  // [cap][warps][NV]
   float* nred = reinterpret_cast<float*>(smem + L.nred);
-  float* xch = reinterpret_cast<float*>(smem + L.xch);   // [rounds][C-1][NV] (rank 0)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t rank = 0, cl = blockIdx.x;
-  if (a.C > 1) {
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(rank));
-    cl = blockIdx.x / a.C;
-  }
+  const int ks = blockIdx.x % a.C;                // this CTA's K slice
   const int n_rg = a.n_rb / R;
-  const int sg0 = (int)rank * a.spc;
+  const int sg0 = ks * a.spc;
   const int sg1 = min(a.S, sg0 + a.spc);
-  const int nsg = max(0, sg1 - sg0);
-  const int nch = (nsg + a.csg - 1) / a.csg;  // ring items per row group
-  const int units = (int)cl < n_rg ? (n_rg - 1 - (int)cl) / a.n_cl + 1 : 0;
-  const int n_items = units * nch;
+  const int nch = (max(0, sg1 - sg0) + a.csg - 1) / a.csg;  // ring items per row group
   const int kc = a.spc * F::SGK;
   const int k0 = sg0 * F::SGK;
   const int k1 = min(a.K, sg1 * F::SGK);
@@ -358,200 +458,176 @@ __global__ void __launch_bounds__(kSgThreads, 2) gemv_s_kernel(const GemvSArgs a
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSgWarps);
     }
-    for (int r = 0; r < a.rounds; ++r) mbar_init(&rbar[r], 1);
+    mbar_init(done, 1);
     *abort_s = 0;
     *cfail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    // rank 0 expects the other ranks' sums of every row group it owns
-    if (a.C > 1 && rank == 0)
-      for (int u = 0; u < units; ++u) mbar_expect_tx(&rbar[u], (uint32_t)((a.C - 1) * NV * 4));
   }
-  if (a.C > 1) {
-    // every rank's barriers are initialised before any rank pushes into them
-    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
 
+  if (warp > kSgWarps) {  // padding: stay resident until the compute warps are done
+    if (lane == 0) sg_wait(done, 0, nullptr);
+    return;
+  }
   if (warp == kSgWarps) {
     // ---------------- producer: weights only (no dependency on the previous kernel)
     if (lane == 0) {
-      int issued = 0;
-      for (int it = 0; it < n_items; ++it) {
-        const int s = it % a.slots, ph = it / a.slots;
-        if (ph > 0 && !sg_wait(&empty[s], (ph - 1) & 1, abort_s)) {
-          if (!*abort_s) { set_err(a.err, G4_DEV_TIMEOUT); *abort_s = 1; }
-          break;
-        }
-        if (*abort_s) break;
-        const int u = it / nch, c = it - u * nch;
-        const int rg = (int)cl + u * a.n_cl;
-        const int cs0 = sg0 + c * a.csg;
-        const int ncs = min(sg1, cs0 + a.csg) - cs0;
-        uint8_t* dst = ring + (size_t)s * a.slot_bytes;
-        mbar_expect_tx(&full[s], (uint32_t)(R * ncs * (kSgW + kSgS)));
+      int it = 0;
+      bool dead = false;
+      auto slot_free = [&](int s, int ph) {  // the consumers released the slot's previous item
+        if (ph == 0) return true;
+        if (sg_wait(&empty[s], (ph - 1) & 1, abort_s)) return true;
+        if (!*abort_s) { set_err(a.err, G4_DEV_TIMEOUT); *abort_s = 1; }
+        return false;
+      };
+      for (int u = 0; u < a.cap && !dead; ++u) {
+        // take the next row group only once the ring has room for its first item
+        if (!slot_free(it % a.slots, it / a.slots)) { dead = true; break; }
+        const int rg = (int)atomicAdd(&a.grab[ks], 1u);
+        if (rg >= n_rg) break;
+        unit_rg[u] = rg;
+        for (int c = 0; c < nch; ++c, ++it) {
+          const int s = it % a.slots, ph = it / a.slots;
+          if (c > 0 && !slot_free(s, ph)) { dead = true; break; }
+          const int cs0 = sg0 + c * a.csg;
+          const int ncs = min(sg1, cs0 + a.csg) - cs0;
+          uint8_t* dst = ring + (size_t)s * a.slot_bytes;
+          tag[s] = u;
+          mbar_expect_tx(&full[s], (uint32_t)(R * ncs * (kSgW + kSgS)));  // releases tag and unit_rg
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const size_t rb = (size_t)rg * R + r;
-          bulk_g2s(dst + r * ncs * kSgW, a.qw + (rb * a.tiles + (size_t)cs0 * 8) * 32, ncs * kSgW, &full[s]);
-          if constexpr (W4)
-            bulk_g2s(dst + R * ncs * kSgW + r * ncs * kSgS, a.sc + (rb * a.S + cs0) * 32, ncs * kSgS, &full[s]);
+          for (int r = 0; r < R; ++r) {
+            const size_t rb = (size_t)rg * R + r;
+            bulk_g2s(dst + r * ncs * kSgW, a.qw + (rb * a.tiles + (size_t)cs0 * 8) * 32, ncs * kSgW, &full[s]);
+            if constexpr (W4)
+              bulk_g2s(dst + R * ncs * kSgW + r * ncs * kSgS, a.sc + (rb * a.S + cs0) * 32, ncs * kSgS, &full[s]);
+          }
         }
-        ++issued;
       }
-      // no copy may be in flight into this CTA's shared memory when it exits
-      for (int it = max(0, issued - a.slots); it < issued; ++it) sg_wait(&full[it % a.slots], (it / a.slots) & 1, nullptr);
+      // the slice's counters go back to zero once every CTA of the slice has stopped taking
+      __threadfence();
+      if (atomicAdd(&a.done[ks], 1u) == gridDim.x / a.C - 1) {
+        atomicExch(&a.grab[ks], 0u);
+        atomicExch(&a.done[ks], 0u);
+      }
+      // end mark for the consumers (an item without data)
+      bool marked = false;
+      if (!dead && slot_free(it % a.slots, it / a.slots)) {
+        tag[it % a.slots] = -1;
+        mbar_arrive(&full[it % a.slots]);
+        marked = true;
+      }
+      // No copy may be in flight into this CTA's shared memory when it exits: wait for the last
+      // item of every slot.  The end mark's slot held item it - slots, which the consumers had
+      // released (so it had landed) before the mark went in; its barrier is a phase further on.
+      for (int j = max(0, it - a.slots); j < it; ++j)
+        if (!(marked && j == it - a.slots)) sg_wait(&full[j % a.slots], (j / a.slots) & 1, nullptr);
+      sg_wait(done, 0, nullptr);
     }
     return;
   }
 
   // ---------------- compute warps
-  if (units == 0) return;
+  struct DoneOnExit {  // lets the producer leave on every way out of the compute warps
+    uint64_t* b;
+    __device__ ~DoneOnExit() {
+      if (threadIdx.x == 0) mbar_arrive(b);
+    }
+  } done_on_exit{done};
   sg_stage_gains(a, stage, NB);  // weights: before the dependency wait
   pdl_wait();
   pdl_trigger();
   sg_prologue<NB>(a, xs, stage, nred, kc, k0, k1);
   // A failed wait is recorded in cfail before the next barrier of the compute warps and acted
   // on after it, so every warp leaves at the same point (no warp is left at a barrier).
+  int units = 0;
   bool ok = true;
-  for (int u = 0; u < units; ++u) {
-    float2 acc[R][NB];
+  float2 acc[R][NB];
+  for (int it = 0; ok; ++it) {
+    const int s = it % a.slots, ph = it / a.slots;
+    if (!sg_wait(&full[s], ph & 1, nullptr)) {
+      ok = false;
+      if (lane == 0) { set_err(a.err, G4_DEV_TIMEOUT); *cfail = 1; *abort_s = 1; }
+      break;
+    }
+    const int u = tag[s];
+    if (u < 0) break;  // no more row groups
+    const int c = it - u * nch;
+    if (c == 0) {
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+      for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
-    for (int c = 0; c < nch && ok; ++c) {
-      const int it = u * nch + c, s = it % a.slots, ph = it / a.slots;
-      if (!sg_wait(&full[s], ph & 1, nullptr)) {
-        ok = false;
-        if (lane == 0) { set_err(a.err, G4_DEV_TIMEOUT); *cfail = 1; *abort_s = 1; }
-        break;
-      }
-      const int cs0 = sg0 + c * a.csg;
-      const int ncs = min(sg1, cs0 + a.csg) - cs0;
-      const uint8_t* src = ring + (size_t)s * a.slot_bytes;
-      // this warp's tiles of the item: tile warp of supergroup j of each row block (j < ncs);
-      // all loads first, then the arithmetic
-      uint4 wv[kSgMaxCsg][R];
-      uint32_t s2[kSgMaxCsg][R];
+        for (int b = 0; b < NB; ++b) acc[r][b] = make_float2(0.f, 0.f);
+    }
+    const int cs0 = sg0 + c * a.csg;
+    const int ncs = min(sg1, cs0 + a.csg) - cs0;
+    const uint8_t* src = ring + (size_t)s * a.slot_bytes;
+    // this warp's tiles of the item: tile `warp` of supergroup j of each row block (j < ncs);
+    // all loads first, then the arithmetic
+    uint4 wv[kSgMaxCsg][R];
+    uint32_t s2[kSgMaxCsg][R];
 #pragma unroll
-      for (int j = 0; j < kSgMaxCsg; ++j) {
-        if (j < ncs) {
-          const int i = warp + 8 * j;
+    for (int j = 0; j < kSgMaxCsg; ++j) {
+      if (j < ncs) {
+        const int i = warp + 8 * j;
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            wv[j][r] = *reinterpret_cast<const uint4*>(src + ((size_t)(r * ncs * 8 + i) * 32 + lane) * 16);
-            s2[j][r] = 0;
-            if constexpr (W4) {
-              const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + R * ncs * kSgW + (r * ncs + j) * kSgS +
-                                                                     lane * 16 + (warp >> 1) * 4);
-              const uint32_t hh = (warp & 1) ? (sw >> 16) : (sw & 0xFFFFu);
-              s2[j][r] = hh | (hh << 16);
-            }
+        for (int r = 0; r < R; ++r) {
+          wv[j][r] = *reinterpret_cast<const uint4*>(src + ((size_t)(r * ncs * 8 + i) * 32 + lane) * 16);
+          s2[j][r] = 0;
+          if constexpr (W4) {
+            const uint32_t sw = *reinterpret_cast<const uint32_t*>(src + R * ncs * kSgW + (r * ncs + j) * kSgS +
+                                                                   lane * 16 + (warp >> 1) * 4);
+            const uint32_t hh = (warp & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+            s2[j][r] = hh | (hh << 16);
           }
         }
       }
-#pragma unroll
-      for (int j = 0; j < kSgMaxCsg; ++j) {
-        if (j < ncs) {
-          const float* xt = xs + (cs0 - sg0 + j) * F::SGK + warp * F::TK;
-          tiles_fma<FMT, NB, R>(wv[j], s2[j], xt, kc, acc);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // this warp's sums of row group u (its own slot: no barrier between row groups)
-    float* rb = red + (size_t)u * kSgWarps * NV;
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-#pragma unroll
-      for (int b = 0; b < NB; ++b) rb[warp * NV + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
-  }
-  sg_csync();
-  // threads add four values of a row group over the warps in warp order and keep (rank 0) or
-  // push (other ranks) them
-  for (int e = threadIdx.x; e < units * (NV / 4) && !*cfail; e += kSgWarps * 32) {
-    const int u = e / (NV / 4), q = e - u * (NV / 4);
-    const float* rb = red + (size_t)u * kSgWarps * NV;
-    {
-      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kSgWarps; ++w) {
-        const float4 v = reinterpret_cast<const float4*>(rb + w * NV)[q];
-        sum.x += v.x;
-        sum.y += v.y;
-        sum.z += v.z;
-        sum.w += v.w;
-      }
-      if (a.C > 1 && rank != 0) {
-        const uint32_t la = sg_su32(xch + ((size_t)(u * (a.C - 1) + rank - 1) * NV + 4 * q));
-        const uint32_t lb = sg_su32(&rbar[u]);
-        uint32_t ra, rbr;
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(la), "r"(0));
-        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(rbr) : "r"(lb), "r"(0));
-        asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
-                         ra),
-                     "f"(sum.x), "f"(sum.y), "f"(sum.z), "f"(sum.w), "r"(rbr)
-                     : "memory");
-      } else {
-        reinterpret_cast<float4*>(fin + u * NV)[q] = sum;
+    for (int j = 0; j < kSgMaxCsg; ++j) {
+      if (j < ncs) {
+        const float* xt = xs + (cs0 - sg0 + j) * F::SGK + warp * F::TK;
+        tiles_fma<FMT, NB, R>(wv[j], s2[j], xt, kc, acc);
       }
     }
-  }
-  sg_csync();  // fin is read below by other threads
-  if (*cfail || (a.C > 1 && rank != 0)) {
-    if (*cfail && a.C > 1 && rank == 0 && threadIdx.x == 0) {
-      // other ranks may still push: leave only after every row group's pushes landed (bounded)
-      for (int u = 0; u < units; ++u) sg_wait(&rbar[u], 0, nullptr);
-    }
-    return;
-  }
-  if (a.C > 1 && threadIdx.x < NV / 4) {
-    // add the other ranks' sums in rank order
-    const int q = threadIdx.x;
-    for (int u = 0; u < units; ++u) {
-      if (!sg_wait(&rbar[u], 0, nullptr)) {
-        set_err(a.err, G4_DEV_TIMEOUT);
-        *cfail = 1;
-        break;
-      }
-      float4 sum = reinterpret_cast<const float4*>(fin + u * NV)[q];
-      for (int o = 0; o < a.C - 1; ++o) {
-        const float4 v = reinterpret_cast<const float4*>(xch + (size_t)(u * (a.C - 1) + o) * NV)[q];
-        sum.x += v.x;
-        sum.y += v.y;
-        sum.z += v.z;
-        sum.w += v.w;
-      }
-      reinterpret_cast<float4*>(fin + u * NV)[q] = sum;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (c == nch - 1) {
+      // this warp's sums of unit u (its own slot: no barrier between row groups)
+      float* rb = red + (size_t)u * kSgWarps * NV;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int b = 0; b < NB; ++b) rb[warp * NV + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
+      units = u + 1;
     }
   }
   sg_csync();
-  if (*cfail) {
-    if (threadIdx.x == 0)
-      for (int u = 0; u < units; ++u) sg_wait(&rbar[u], 0, nullptr);
-    return;
-  }
-  // epilogues: value v = (r * NB + b) * 32 + lane of row group u is output row
-  // (rg * R + r) * 32 + lane of batch row b
+  if (*cfail) return;
+  // outputs: value v = (r * NB + b) * 32 + lane of unit u is row (rg * R + r) * 32 + lane of
+  // batch row b, summed over the warps in warp order
+  float* ys = a.y + (size_t)ks * a.y_part_stride;
   for (int e = threadIdx.x; e < units * NV; e += kSgWarps * 32) {
     const int u = e / NV, v = e - u * NV;
     const int ln = v & 31, rbk = v >> 5, b = rbk % NB, r = rbk / NB;
     if (b >= a.nb) continue;
-    const int rg = (int)cl + u * a.n_cl;
-    const float* f = fin + u * NV;
+    const int rg = unit_rg[u];
+    const float* rb = red + (size_t)u * kSgWarps * NV;
+    auto sum_of = [&](int vv) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSgWarps; ++w) sum += rb[w * NV + vv];
+      return sum;
+    };
     if constexpr (EPI == EPI_GEGLU) {
       if (r != 0) continue;
       const int n = rg * 32 + ln;  // R == 2: block 0 = gate rows, block 1 = up rows
-      if (n < a.n_valid) a.y[(size_t)b * a.y_stride + n] = gelu_tanh(f[(0 * NB + b) * 32 + ln]) * f[(1 * NB + b) * 32 + ln];
+      if (n < a.n_valid) ys[(size_t)b * a.y_stride + n] = gelu_tanh(sum_of(v)) * sum_of(v + NB * 32);
     } else {
       const int n = (rg * R + r) * 32 + ln;
       if (n >= a.n_valid) continue;
-      float val = f[v];
+      float val = sum_of(v);
       if constexpr (EPI == EPI_PLE) val = gelu_tanh(val) * a.ple[(size_t)b * a.ple_stride + n];
-      a.y[(size_t)b * a.y_stride + n] = val;
+      ys[(size_t)b * a.y_stride + n] = val;
     }
   }
 }

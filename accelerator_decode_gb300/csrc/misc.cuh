@@ -53,8 +53,10 @@ __global__ void embed_kernel(const EmbedArgs a) {
 
 // ple[b][l] = (RMSNorm(pr[b][l] * H^-1/2) * g + tok[b][l]) * 2^-1/2, one block per (b, l).
 // "Porting Gemma 4 E2B to SGLang-JAX", Step 3 (per-layer projection norm and the combine).
-__global__ void ple_combine_kernel(const float* pr, const float* tok, const __nv_bfloat16* g, int L, int P,
-                                   float inv_sqrt_h, float inv_sqrt2, float eps, float* ple) {
+// pr may come as `parts` K-slice partial sums (part q at pr + q * part_stride), added in order.
+__global__ void ple_combine_kernel(const float* pr, int parts, long part_stride, const float* tok,
+                                   const __nv_bfloat16* g, int L, int P, float inv_sqrt_h, float inv_sqrt2, float eps,
+                                   float* ple) {
   __shared__ float red[32];
   pdl_wait();
   pdl_trigger();
@@ -62,13 +64,17 @@ __global__ void ple_combine_kernel(const float* pr, const float* tok, const __nv
   const size_t base = ((size_t)b * L + l) * P;
   float ss[1] = {0.f};
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
-    const float v = pr[base + i] * inv_sqrt_h;
+    float v = __ldcg(pr + base + i);
+    for (int q = 1; q < parts; ++q) v += __ldcg(pr + q * part_stride + base + i);
+    v *= inv_sqrt_h;
     ss[0] += v * v;
   }
   block_sum<1>(ss, red);
   const float den = rms_denom(ss[0], P, eps);
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
-    const float v = pr[base + i] * inv_sqrt_h;
+    float v = __ldcg(pr + base + i);
+    for (int q = 1; q < parts; ++q) v += __ldcg(pr + q * part_stride + base + i);
+    v *= inv_sqrt_h;
     ple[base + i] = ((v / den) * bf16f(g[i]) + tok[base + i]) * inv_sqrt2;
   }
 }
