@@ -2,10 +2,17 @@
 //
 // Per sequence b at position p, for the query heads of one head group:
 //   q_h = RoPE(RMSNorm(q_raw_h) * g_q)                      (every layer)
-//   owning layers: k = bf16(RoPE(RMSNorm(k_raw) * g_k)), v = bf16(v_raw) written in place
-//   at cache row (slot, p) -- a sharing layer applies RoPE to its queries only and reads
-//   its source layer's cache ("Porting Gemma 4 E2B to SGLang-JAX", Step 4; "One TPU chip,
-//   eight agents", The engine: kv_share_map, static cache written in place).
+//   owning layers: k = RoPE(RMSNorm(k_raw) * g_k), v = v_raw written in place at cache row
+//   (slot, p) -- a sharing layer applies RoPE to its queries only and reads its source
+//   layer's cache ("Porting Gemma 4 E2B to SGLang-JAX", Step 4; "One TPU chip, eight
+//   agents", The engine: kv_share_map, static cache written in place).
+// Cache rows are bf16, or int8 codes with one fp32 scale per row ("One TPU chip, eight
+// agents", Measured: the raw JAX decode kernel, int8 KV cache): s = max|r| / 127,
+// c = round-half-even(r / s) clipped to +-127, stored value c * s.  With int8 rows the row
+// scale is applied once per key (to the score, and to the softmax weight of the value row).
+// Row addresses are static (slot * max_context + position) or paged: page_table[slot][p /
+// page_size] names the pool page that holds positions [p - p % page_size, +page_size)
+// ("Six serving engines on one Cloud TPU v5e chip", Step 3, page size 128).
 //   keys j in [lo, p], lo = 0 (full) or max(0, p - W + 1) (sliding window W);
 //   s_j = scale * q_h . K_j; o_h = sum_j softmax(s)_j V_j  (fp32, max-subtracted).
 // The visible keys are cut into nsplit chunks (one CTA each), staged through shared memory
@@ -29,8 +36,13 @@ struct AttnArgs {
   float scale;
   int window;              // 0 = full attention
   int own;                 // write K/V of this position
-  __nv_bfloat16* kc;       // cache of the source layer [max_batch][t_max][D]
-  __nv_bfloat16* vc;
+  void* kc;                // cache of the source layer: rows of D bf16 or D int8 (KV8)
+  void* vc;
+  float* ksc;              // KV8: fp32 scale per row
+  float* vsc;
+  const int* page_table;   // paged: [max_batch][max_pages] pool page per page of positions; NULL: static
+  int page_shift;          // log2(page size)
+  int max_pages;
   int t_max;
   int max_batch;
   const float* rope_cos;   // [t_max][D/2]
@@ -47,11 +59,39 @@ struct AttnArgs {
   int* err;
 };
 
-template <int D, int HPC>
+template <int D, int HPC, bool KV8 = false>
 __host__ __device__ inline size_t attn_smem_bytes(int nstage) {
-  return (size_t)nstage * 2 * kAttnTile * D * 2                      // K, V tiles (bf16)
+  return (size_t)nstage * 2 * kAttnTile * D * (KV8 ? 1 : 2)          // K, V tiles
+         + (KV8 ? (size_t)nstage * 2 * kAttnTile * 4 : 0)            // their row scales
          + ((size_t)HPC * D + 2 * D + HPC * kAttnTile + 4 * HPC) * 4   // q, new k/v, scores, stats
-         + (64 + 4) * 4;                                             // merge weights, last flag
+         + (64 + 4 + 4) * 4;                                         // merge weights, last flag, new scales
+}
+
+// Cache row of (slot, position j): static, or through the slot's page table; -1 when the
+// position has no page.
+__device__ __forceinline__ long kv_row_index(const AttnArgs& a, int slot, int j) {
+  if (!a.page_table) return (long)slot * a.t_max + j;
+  const int pg = __ldg(a.page_table + (size_t)slot * a.max_pages + (j >> a.page_shift));
+  return pg < 0 ? -1L : ((long)pg << a.page_shift) + (j & ((1 << a.page_shift) - 1));
+}
+
+// Byte i of w as a signed int8 code, exactly, as fp32 (offset binary in a float's mantissa).
+__device__ __forceinline__ float i8f(uint32_t w, int i) {
+  return __uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | i)) - 8388736.f;
+}
+
+// int8 code of a row of D values spread over a warp (element lane + 32 e in v[e]):
+// s = max|v| / 127, c = rint(v / s) clipped to +-127 (0 for an all-zero row).
+template <int D>
+__device__ __forceinline__ float kv_quant_row(float (&v)[D / 32], int8_t (&c)[D / 32]) {
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) m = fmaxf(m, fabsf(v[e]));
+  m = warp_max(m);
+  const float s = m / 127.f;
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) c[e] = s > 0.f ? (int8_t)fminf(fmaxf(rintf(v[e] / s), -127.f), 127.f) : (int8_t)0;
+  return s;
 }
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
@@ -59,11 +99,13 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 }
 
 // New K/V row of an owning layer at position p, on one warp: k = RoPE(RMSNorm(k) g_k), v,
-// both rounded to bf16.  Stores the row in the cache when `store`; copies the rounded values
-// to knew / vnew (shared, [D]) when they are given.  cs / sn: this lane's RoPE factors at p.
-template <int D>
+// rounded to bf16 or coded to int8.  Stores the row in the cache when `store`; copies the
+// stored values to knew / vnew (shared, [D]) when they are given -- for int8 rows the codes,
+// with the two row scales in kvs_new[0..1].  cs / sn: this lane's RoPE factors at p.
+template <int D, bool KV8>
 __device__ __forceinline__ void kv_row(const AttnArgs& a, const float* qraw, int slot, int p, const float (&cs)[D / 64],
-                                       const float (&sn)[D / 64], float* knew, float* vnew, bool store) {
+                                       const float (&sn)[D / 64], float* knew, float* vnew, float* kvs_new,
+                                       bool store) {
   const int lane = threadIdx.x & 31;
   const float* kr = qraw + (size_t)a.nq * D;
   const float* vr = kr + D;
@@ -81,28 +123,50 @@ __device__ __forceinline__ void kv_row(const AttnArgs& a, const float* qraw, int
   const float den = rms_denom(ss, D, a.eps);
 #pragma unroll
   for (int e = 0; e < D / 32; ++e) kv_[e] = (kv_[e] / den) * gk[e];
-  __nv_bfloat16* kdst = a.kc + ((size_t)slot * a.t_max + p) * D;
-  __nv_bfloat16* vdst = a.vc + ((size_t)slot * a.t_max + p) * D;
+  // RoPE pairs element i with i + D/2: for i = lane + 32 e (e < D/64) the partner is in
+  // kv_[e + D/64] of the same lane
 #pragma unroll
   for (int e = 0; e < D / 64; ++e) {
-    const int i = lane + 32 * e;
     const float ka = kv_[e], kb = kv_[e + D / 64];
-    const __nv_bfloat16 k1 = __float2bfloat16_rn(ka * cs[e] - kb * sn[e]);
-    const __nv_bfloat16 k2 = __float2bfloat16_rn(kb * cs[e] + ka * sn[e]);
-    if (knew) { knew[i] = bf16f(k1); knew[i + D / 2] = bf16f(k2); }
-    if (store) { kdst[i] = k1; kdst[i + D / 2] = k2; }
+    kv_[e] = ka * cs[e] - kb * sn[e];
+    kv_[e + D / 64] = kb * cs[e] + ka * sn[e];
   }
+  const long row = kv_row_index(a, slot, p);
+  if (row < 0) {
+    if (store && lane == 0) set_err(a.err, G4_DEV_BAD_POSITION);
+    store = false;
+  }
+  if constexpr (KV8) {
+    int8_t kc8[D / 32], vc8[D / 32];
+    const float sk = kv_quant_row<D>(kv_, kc8);
+    const float sv = kv_quant_row<D>(vv_, vc8);
+    int8_t* kdst = reinterpret_cast<int8_t*>(a.kc) + (size_t)(row < 0 ? 0 : row) * D;
+    int8_t* vdst = reinterpret_cast<int8_t*>(a.vc) + (size_t)(row < 0 ? 0 : row) * D;
 #pragma unroll
-  for (int e = 0; e < D / 32; ++e) {
-    const __nv_bfloat16 v1 = __float2bfloat16_rn(vv_[e]);
-    if (vnew) vnew[lane + 32 * e] = bf16f(v1);
-    if (store) vdst[lane + 32 * e] = v1;
+    for (int e = 0; e < D / 32; ++e) {
+      if (knew) { knew[lane + 32 * e] = (float)kc8[e]; vnew[lane + 32 * e] = (float)vc8[e]; }
+      if (store) { kdst[lane + 32 * e] = kc8[e]; vdst[lane + 32 * e] = vc8[e]; }
+    }
+    if (lane == 0) {
+      if (kvs_new) { kvs_new[0] = sk; kvs_new[1] = sv; }
+      if (store) { a.ksc[row] = sk; a.vsc[row] = sv; }
+    }
+  } else {
+    __nv_bfloat16* kdst = reinterpret_cast<__nv_bfloat16*>(a.kc) + (size_t)(row < 0 ? 0 : row) * D;
+    __nv_bfloat16* vdst = reinterpret_cast<__nv_bfloat16*>(a.vc) + (size_t)(row < 0 ? 0 : row) * D;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+      const __nv_bfloat16 k1 = __float2bfloat16_rn(kv_[e]);
+      const __nv_bfloat16 v1 = __float2bfloat16_rn(vv_[e]);
+      if (knew) { knew[lane + 32 * e] = bf16f(k1); vnew[lane + 32 * e] = bf16f(v1); }
+      if (store) { kdst[lane + 32 * e] = k1; vdst[lane + 32 * e] = v1; }
+    }
   }
 }
 
 // One (split, head group, sequence) unit on kAttnThreads threads; `asmem` holds
 // attn_smem_bytes<D, HPC>(a.nstage) bytes.  Called by attn_kernel and by the persistent step.
-template <int D, int HPC>
+template <int D, int HPC, bool KV8 = false>
 // Threads [tid_base, tid_base + 128) run the unit and synchronise on named barrier bar_id.
 __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, int b, unsigned char* asmem,
                                           int tid_base, int bar_id) {
@@ -110,9 +174,12 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   constexpr int PT = D >= kAttnThreads ? D / kAttnThreads : 1;  // output elements per thread
   static_assert(PL >= 2 && PL % 2 == 0, "head dim must be a multiple of 64");
   constexpr int TD = kAttnTile * D;
-  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(asmem);  // [nstage][TILE][D]
-  __nv_bfloat16* Vs = Ks + (size_t)a.nstage * TD;                // [nstage][TILE][D]
-  float* qs = reinterpret_cast<float*>(Vs + (size_t)a.nstage * TD);  // [HPC][D]
+  constexpr int EB = KV8 ? 1 : 2;                               // bytes per cached value
+  unsigned char* Ks = asmem;                                    // [nstage][TILE][D] values
+  unsigned char* Vs = Ks + (size_t)a.nstage * TD * EB;
+  float* Kss = reinterpret_cast<float*>(Vs + (size_t)a.nstage * TD * EB);  // KV8: [nstage][TILE] row scales
+  float* Vss = Kss + (KV8 ? a.nstage * kAttnTile : 0);
+  float* qs = Vss + (KV8 ? a.nstage * kAttnTile : 0);          // [HPC][D]
   float* knew = qs + HPC * D;
   float* vnew = knew + D;
   float* sc = vnew + D;          // [HPC][TILE]
@@ -121,6 +188,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   float* l_sh = m_sh + HPC;
   float* wgt = l_sh + 2 * HPC;                           // [64]
   int* is_last_p = reinterpret_cast<int*>(wgt + 64);
+  float* kvs_new = wgt + 68;                             // KV8: scales of the new K and V rows
 
   const int tid = threadIdx.x - tid_base, warp = tid >> 5, lane = tid & 31;
   const int h0 = hg * HPC;
@@ -139,20 +207,35 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   const int j1 = min(p + 1, j0 + chunk);
   const bool has_p = (p >= 0) && (j0 <= p) && (p < j1);
   const int ntiles = j1 > j0 ? (j1 - j0 + kAttnTile - 1) / kAttnTile : 0;
-  const __nv_bfloat16* kbase = a.kc + (size_t)(slot < 0 ? 0 : slot) * a.t_max * D;
-  const __nv_bfloat16* vbase = a.vc + (size_t)(slot < 0 ? 0 : slot) * a.t_max * D;
+  const unsigned char* kbase = reinterpret_cast<const unsigned char*>(a.kc);
+  const unsigned char* vbase = reinterpret_cast<const unsigned char*>(a.vc);
+  const int slot0 = slot < 0 ? 0 : slot;
 
-  // tile loader: keys [t0, t0 + 32) clipped to j1; rows past it are zero-filled
+  // tile loader: keys [t0, t0 + 32) clipped to j1; rows past it (or without a page) are
+  // zero-filled, with zero scales
   auto load_tile = [&](int ti) {
     const int t0 = j0 + ti * kAttnTile;
     const int st = ti % a.nstage;
-    constexpr int C8 = D / 8;  // 16-byte chunks per row
-    for (int i = tid; i < kAttnTile * C8; i += kAttnThreads) {
-      const int r = i / C8, c = i - r * C8;
-      const bool ok = t0 + r < j1;
-      const size_t off = (size_t)(ok ? t0 + r : 0) * D + 8 * c;
-      cp_async16(Ks + (size_t)st * TD + r * D + 8 * c, kbase + off, ok);
-      cp_async16(Vs + (size_t)st * TD + r * D + 8 * c, vbase + off, ok);
+    constexpr int CR = D * EB / 16;  // 16-byte chunks per row
+    for (int i = tid; i < kAttnTile * CR; i += kAttnThreads) {
+      const int r = i / CR, c = i - r * CR;
+      const long row = t0 + r < j1 ? kv_row_index(a, slot0, t0 + r) : -1L;
+      const bool ok = row >= 0;
+      if (!ok && c == 0 && t0 + r < j1) set_err(a.err, G4_DEV_BAD_POSITION);  // no page
+      const size_t off = (size_t)(ok ? row : 0) * D * EB + 16 * c;
+      cp_async16(Ks + ((size_t)st * TD + r * D) * EB + 16 * c, kbase + off, ok);
+      cp_async16(Vs + ((size_t)st * TD + r * D) * EB + 16 * c, vbase + off, ok);
+      if constexpr (KV8) {
+        if (c == 0) {
+          if (ok) {
+            cp_async4(Kss + st * kAttnTile + r, a.ksc + row);
+            cp_async4(Vss + st * kAttnTile + r, a.vsc + row);
+          } else {
+            Kss[st * kAttnTile + r] = 0.f;
+            Vss[st * kAttnTile + r] = 0.f;
+          }
+        }
+      }
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
   };
@@ -203,7 +286,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
     }
   }
   // ---- new K/V row of an owning layer (position p), computed by every CTA holding key p
-  if (use_new && warp == kKvWarp) kv_row<D>(a, qraw, slot, p, cs, sn, knew, vnew, hg == 0);
+  if (use_new && warp == kKvWarp) kv_row<D, KV8>(a, qraw, slot, p, cs, sn, knew, vnew, kvs_new, hg == 0);
 
   // ---- tiles with online softmax
   float m_run[HPC], l_run[HPC];
@@ -222,8 +305,8 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
     if (a.nstage > 1 && ti + 1 < ntiles) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
     else asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     named_sync(bar_id, kAttnThreads);
-    const __nv_bfloat16* Kt = Ks + (size_t)st * TD;
-    const __nv_bfloat16* Vt = Vs + (size_t)st * TD;
+    const unsigned char* Kt = Ks + (size_t)st * TD * EB;
+    const unsigned char* Vt = Vs + (size_t)st * TD * EB;
     // scores: warp per key, lanes over D.  A warp's keys (jj = warp + 4 q) are dotted first and
     // reduced together, so the shuffle chains overlap; zero-filled rows past tn are skipped.
     constexpr int KPW = kAttnTile / (kAttnThreads / 32);
@@ -244,10 +327,24 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
       if (use_new && j == p) {
 #pragma unroll
         for (int e = 0; e < PL; ++e) kv[e] = knew[lane * PL + e];
+      } else if constexpr (KV8) {
+        const unsigned char* kp = Kt + jj * D + lane * PL;
+        if constexpr (PL % 4 == 0) {
+#pragma unroll
+          for (int c = 0; c < PL / 4; ++c) {
+            const uint32_t w = reinterpret_cast<const uint32_t*>(kp)[c];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) kv[4 * c + m] = i8f(w, m);
+          }
+        } else {
+          const uint32_t w = *reinterpret_cast<const uint16_t*>(kp);
+#pragma unroll
+          for (int m = 0; m < PL; ++m) kv[m] = i8f(w, m);
+        }
       } else if constexpr (PL % 8 == 0) {
 #pragma unroll
         for (int c = 0; c < PL / 8; ++c) {
-          const uint4 u = reinterpret_cast<const uint4*>(Kt + jj * D + lane * PL)[c];
+          const uint4 u = reinterpret_cast<const uint4*>(Kt + (jj * D + lane * PL) * 2)[c];
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int m = 0; m < 4; ++m) { kv[c * 8 + 2 * m] = bf16_lo(w[m]); kv[c * 8 + 2 * m + 1] = bf16_hi(w[m]); }
@@ -255,7 +352,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
       } else {
 #pragma unroll
         for (int c = 0; c < PL / 2; ++c) {
-          const uint32_t w = reinterpret_cast<const uint32_t*>(Kt + jj * D + lane * PL)[c];
+          const uint32_t w = reinterpret_cast<const uint32_t*>(Kt + (jj * D + lane * PL) * 2)[c];
           kv[2 * c] = bf16_lo(w);
           kv[2 * c + 1] = bf16_hi(w);
         }
@@ -282,7 +379,11 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
       for (int q = 0; q < KPW; ++q) {
         const int jj = warp + q * (kAttnThreads / 32);
 #pragma unroll
-        for (int h = 0; h < HPC; ++h) sc[h * kAttnTile + jj] = (jj < tn) ? dq[h][q] * a.scale : -INFINITY;
+        for (int h = 0; h < HPC; ++h) {
+          float s_ = dq[h][q] * a.scale;
+          if constexpr (KV8) s_ *= (use_new && t0 + jj == p) ? kvs_new[0] : Kss[st * kAttnTile + jj];
+          sc[h * kAttnTile + jj] = (jj < tn) ? s_ : -INFINITY;
+        }
       }
     }
     named_sync(bar_id, kAttnThreads);
@@ -296,7 +397,10 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
       const float pj = (lane < tn) ? expf(s - mn) : 0.f;
       const float ls = warp_sum(pj);
       const float r = expf(m_run[h] - mn);  // 0 on the first tile
-      sc[h * kAttnTile + lane] = pj;
+      if constexpr (KV8)  // the value row's scale rides on its weight
+        sc[h * kAttnTile + lane] = pj * ((use_new && t0 + lane == p) ? kvs_new[1] : Vss[st * kAttnTile + lane]);
+      else
+        sc[h * kAttnTile + lane] = pj;
       if (lane == 0) resc[h] = r;
       m_run[h] = mn;
       l_run[h] = l_run[h] * r + ls;
@@ -317,8 +421,21 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
         if (use_new && j == p) {
 #pragma unroll
           for (int e = 0; e < PT; ++e) vv[e] = vnew[tid * PT + e];
+        } else if constexpr (KV8) {
+          const unsigned char* vp = Vt + jj * D + tid * PT;
+          if constexpr (PT == 4) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vv[e] = i8f(w, e);
+          } else if constexpr (PT == 2) {
+            const uint32_t w = *reinterpret_cast<const uint16_t*>(vp);
+            vv[0] = i8f(w, 0);
+            vv[1] = i8f(w, 1);
+          } else {
+            vv[0] = i8f(vp[0], 0);
+          }
         } else {
-          const __nv_bfloat16* vp = Vt + jj * D + tid * PT;
+          const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(Vt) + jj * D + tid * PT;
           if constexpr (PT == 1) {
             vv[0] = bf16f(vp[0]);
           } else if constexpr (PT == 2) {
@@ -424,18 +541,18 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   if (tid == 0) a.counters[b * n_hg + hg] = 0u;
 }
 
-template <int D, int HPC>
+template <int D, int HPC, bool KV8>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char asmem_k[];
   pdl_wait();
   pdl_trigger();
-  attn_unit<D, HPC>(a, blockIdx.x, blockIdx.y, blockIdx.z, asmem_k, 0, 1);
+  attn_unit<D, HPC, KV8>(a, blockIdx.x, blockIdx.y, blockIdx.z, asmem_k, 0, 1);
 }
 
 // K/V rows of an owning layer for every row of a step before its attention runs (prefill
 // blocks: rows of one sequence at consecutive positions read each other's keys, so no row
 // may append its own key inside the attention launch).  One warp per row.
-template <int D>
+template <int D, bool KV8>
 __global__ void __launch_bounds__(32) kv_write_kernel(const AttnArgs a) {
   pdl_wait();
   pdl_trigger();
@@ -448,7 +565,7 @@ __global__ void __launch_bounds__(32) kv_write_kernel(const AttnArgs a) {
     cs[e] = __ldg(a.rope_cos + (size_t)p * (D / 2) + lane + 32 * e);
     sn[e] = __ldg(a.rope_sin + (size_t)p * (D / 2) + lane + 32 * e);
   }
-  kv_row<D>(a, a.qkv + (size_t)b * a.qkv_stride, slot, p, cs, sn, nullptr, nullptr, true);
+  kv_row<D, KV8>(a, a.qkv + (size_t)b * a.qkv_stride, slot, p, cs, sn, nullptr, nullptr, nullptr, true);
 }
 
 }  // namespace g4

@@ -119,7 +119,16 @@ struct g4_handle {
   std::vector<Layer> layers;
   Lin pmp, lm;
   const __nv_bfloat16 *embed = nullptr, *ple_table = nullptr, *g_ppn = nullptr, *g_final = nullptr;
-  std::vector<__nv_bfloat16*> kc, vc;  // per owning layer
+  // KV cache per owning layer: rows of d values (bf16, or int8 codes with an fp32 scale per
+  // row in ksc / vsc).  Static rows: slot * max_context + position.  Paged: a pool of n_pages
+  // pages of 2^page_shift rows per layer, one page table for all layers (device copy
+  // page_table [max_batch][max_pages], host mirror pt_host), free pages in free_pages.
+  std::vector<void*> kc, vc;
+  std::vector<float*> ksc, vsc;
+  bool kv8 = false;
+  int* page_table = nullptr;
+  int page_shift = 0, max_pages = 0, n_pages = 0;
+  std::vector<int> pt_host, slot_pages, free_pages;
   float *cos_t[2] = {nullptr, nullptr}, *sin_t[2] = {nullptr, nullptr};
   // activations
   float *x0 = nullptr, *xb[2] = {nullptr, nullptr}, *tok = nullptr, *pr = nullptr, *ple = nullptr;
@@ -370,7 +379,10 @@ void attrs_staged(int optin) {
 }
 template <int D>
 void attrs_attn(int optin) {
-  set_max_dyn(attn_kernel<D, 1>, optin);
+  set_max_dyn(attn_kernel<D, 1, false>, optin);
+  set_max_dyn(attn_kernel<D, 1, true>, optin);
+  carve_max(kv_write_kernel<D, false>);
+  carve_max(kv_write_kernel<D, true>);
 }
 std::mutex g_attr_mu;
 std::map<int, int> g_optin;  // device -> opt-in shared memory bytes
@@ -401,10 +413,6 @@ int init_kernel_attrs(int device) {
   carve_max(ple_combine_kernel);
   carve_max(gather_rows_kernel);
   carve_max(argmax_partials_kernel);
-  carve_max(kv_write_kernel<64>);
-  carve_max(kv_write_kernel<128>);
-  carve_max(kv_write_kernel<256>);
-  carve_max(kv_write_kernel<512>);
   cudaGetLastError();
   g_optin[device] = optin;
   return optin;
@@ -769,15 +777,37 @@ void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const S
 }
 
 // ---------------------------------------------------------------------- attention launch
-template <int D, int HPC>
+template <int D, int HPC, bool KV8>
 void launch_attn(const AttnArgs& a, int nb, cudaStream_t st) {
   dim3 grid(a.nsplit, a.nq / HPC, nb);
-  launch(attn_kernel<D, HPC>, grid, dim3(kAttnThreads), attn_smem_bytes<D, HPC>(a.nstage), st, a);
+  launch(attn_kernel<D, HPC, KV8>, grid, dim3(kAttnThreads), attn_smem_bytes<D, HPC, KV8>(a.nstage), st, a);
 }
 template <int D>
-void launch_attn_d(const AttnArgs& a, int hpc, int nb, cudaStream_t st) {
+void launch_attn_d(const AttnArgs& a, int hpc, int nb, bool kv8, cudaStream_t st) {
   (void)hpc;  // attn_hpc: one head per unit
-  launch_attn<D, 1>(a, nb, st);
+  if (kv8) launch_attn<D, 1, true>(a, nb, st);
+  else launch_attn<D, 1, false>(a, nb, st);
+}
+void launch_attn_any(const AttnArgs& a, int d, int hpc, int nb, bool kv8, cudaStream_t st) {
+  switch (d) {
+    case 64: launch_attn_d<64>(a, hpc, nb, kv8, st); break;
+    case 128: launch_attn_d<128>(a, hpc, nb, kv8, st); break;
+    case 256: launch_attn_d<256>(a, hpc, nb, kv8, st); break;
+    default: launch_attn_d<512>(a, hpc, nb, kv8, st); break;
+  }
+}
+template <int D>
+void launch_kv_write_d(const AttnArgs& a, int nb, bool kv8, cudaStream_t st) {
+  if (kv8) launch(kv_write_kernel<D, true>, dim3(nb), dim3(32), 0, st, a);
+  else launch(kv_write_kernel<D, false>, dim3(nb), dim3(32), 0, st, a);
+}
+void launch_kv_write_any(const AttnArgs& a, int d, int nb, bool kv8, cudaStream_t st) {
+  switch (d) {
+    case 64: launch_kv_write_d<64>(a, nb, kv8, st); break;
+    case 128: launch_kv_write_d<128>(a, nb, kv8, st); break;
+    case 256: launch_kv_write_d<256>(a, nb, kv8, st); break;
+    default: launch_kv_write_d<512>(a, nb, kv8, st); break;
+  }
 }
 
 // Query heads per attention unit.  One: a unit per (split, head, sequence) keeps every unit's
@@ -835,6 +865,16 @@ g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots
 // first layer after which no layer writes K/V on, only rows keep_idx[0 .. n_keep) (their
 // slots and positions in keep_slots / keep_pos) go on: a prompt row that ends no sequence
 // feeds nothing past its last K/V write.  n_keep == 0 ends the step there.
+// Cache of layer Src (its K/V rows, scales and page table) in attention arguments.
+void kv_args(const g4_handle* h, const Layer& Src, AttnArgs& a) {
+  a.kc = h->kc[Src.kv];
+  a.vc = h->vc[Src.kv];
+  a.ksc = h->kv8 ? h->ksc[Src.kv] : nullptr;
+  a.vsc = h->kv8 ? h->vsc[Src.kv] : nullptr;
+  a.page_table = h->page_table;
+  a.page_shift = h->page_shift;
+  a.max_pages = h->max_pages;
+}
 // Attention launch of layer l (shared by both step paths).
 void launch_layer_attn(g4_handle* h, const Layer& Y, const float* qkv, int qkv_stride, int n, const int* d_slots,
                        const int* d_pos, bool own, cudaStream_t st) {
@@ -850,8 +890,7 @@ void launch_layer_attn(g4_handle* h, const Layer& Y, const float* qkv, int qkv_s
   a.scale = Y.scale;
   a.window = Y.full ? 0 : c.sliding_window;
   a.own = own;
-  a.kc = h->kc[Src.kv];
-  a.vc = h->vc[Src.kv];
+  kv_args(h, Src, a);
   a.t_max = c.max_context;
   a.max_batch = c.max_batch;
   a.rope_cos = h->cos_t[Y.full];
@@ -869,12 +908,7 @@ void launch_layer_attn(g4_handle* h, const Layer& Y, const float* qkv, int qkv_s
   a.ws_o = h->attn_o;
   a.counters = h->attn_cnt;
   a.err = h->err;
-  switch (Y.d) {
-    case 64: launch_attn_d<64>(a, hpc, n, st); break;
-    case 128: launch_attn_d<128>(a, hpc, n, st); break;
-    case 256: launch_attn_d<256>(a, hpc, n, st); break;
-    default: launch_attn_d<512>(a, hpc, n, st); break;
-  }
+  launch_attn_any(a, Y.d, hpc, n, h->kv8, st);
 }
 
 // Decode step of 1-4 rows on the staged projections (gemv_s.cuh).  Every projection but the
@@ -1154,8 +1188,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.scale = Y.scale;
       a.window = Y.full ? 0 : c.sliding_window;
       a.own = Y.own && !kv_first;
-      a.kc = h->kc[Src.kv];
-      a.vc = h->vc[Src.kv];
+      kv_args(h, Src, a);
       a.t_max = c.max_context;
       a.max_batch = c.max_batch;
       a.rope_cos = h->cos_t[Y.full];
@@ -1176,20 +1209,8 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.counters = h->attn_cnt;
       a.err = h->err;
       ProfScope ps(prof, Y.full ? "attn.full" : "attn.sliding", 0.0);
-      if (kv_first && Y.own) {
-        switch (Y.d) {
-          case 64: launch(kv_write_kernel<64>, dim3(n), dim3(32), 0, st, a); break;
-          case 128: launch(kv_write_kernel<128>, dim3(n), dim3(32), 0, st, a); break;
-          case 256: launch(kv_write_kernel<256>, dim3(n), dim3(32), 0, st, a); break;
-          default: launch(kv_write_kernel<512>, dim3(n), dim3(32), 0, st, a); break;
-        }
-      }
-      switch (Y.d) {
-        case 64: launch_attn_d<64>(a, hpc, n, st); break;
-        case 128: launch_attn_d<128>(a, hpc, n, st); break;
-        case 256: launch_attn_d<256>(a, hpc, n, st); break;
-        default: launch_attn_d<512>(a, hpc, n, st); break;
-      }
+      if (kv_first && Y.own) launch_kv_write_any(a, Y.d, n, h->kv8, st);
+      launch_attn_any(a, Y.d, hpc, n, h->kv8, st);
       if (h->trace)
         for (int i = 0; i < n; ++i)
           cudaMemcpyAsync(h->trace + ((size_t)(l * 2) * c.max_batch + i) * ts, h->attn + (size_t)i * nqd,
@@ -1338,7 +1359,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, nq = c.num_q_heads;
   const int G = h->sms, NB = 2;
-  if (H % 8) return G4_OK;
+  if (H % 8 || h->kv8) return G4_OK;  // the persistent step reads bf16 cache rows only
   std::vector<MegaPhase> prog;
   size_t smem_f = 64;  // floats
   auto wred_f = [&]() { return (size_t)2 * kMegaWarps * 2 * NB * 32; };  // double-buffered warp partials
@@ -1431,8 +1452,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
       a.scale = Y.scale;
       a.window = Y.full ? 0 : c.sliding_window;
       a.own = Y.own;
-      a.kc = h->kc[Src.kv];
-      a.vc = h->vc[Src.kv];
+      kv_args(h, Src, a);
       a.t_max = c.max_context;
       a.max_batch = c.max_batch;
       a.rope_cos = h->cos_t[Y.full];
@@ -1671,6 +1691,24 @@ g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots
 
 bool is_pow2_dim(int d) { return d == 64 || d == 128 || d == 256 || d == 512; }
 
+// Pages for positions [0, n) of `slot` (paged cache): take the missing ones from the pool and
+// upload the slot's page-table row.
+g4_status kv_reserve_impl(g4_handle* h, cudaStream_t st, int slot, int n) {
+  const int need = cdiv(n, 1 << h->page_shift);
+  int& have = h->slot_pages[slot];
+  if (need <= have) return G4_OK;
+  if (need - have > (int)h->free_pages.size()) return G4_ERR_OOM;
+  int* row = h->pt_host.data() + (size_t)slot * h->max_pages;
+  const int first = have;
+  for (; have < need; ++have) {
+    row[have] = h->free_pages.back();
+    h->free_pages.pop_back();
+  }
+  CK(cudaMemcpyAsync(h->page_table + (size_t)slot * h->max_pages + first, row + first, (need - first) * sizeof(int),
+                     cudaMemcpyHostToDevice, st));
+  return G4_OK;
+}
+
 g4_status validate(const g4_config* c) {
   if (!c) return G4_ERR_INVALID_ARG;
   if (c->num_layers < 1 || c->num_kv_shared_layers < 0 || c->num_kv_shared_layers >= c->num_layers)
@@ -1684,6 +1722,11 @@ g4_status validate(const g4_config* c) {
   if (!is_pow2_dim(c->head_dim_sliding) || !is_pow2_dim(c->head_dim_full)) return G4_ERR_UNSUPPORTED;
   if (c->hidden % 32 || c->mlp % 32 || c->mlp_shared % 32 || c->ple_dim % 32) return G4_ERR_UNSUPPORTED;
   if (c->max_batch > 64 || c->ple_dim > 1024 || c->hidden > 8192) return G4_ERR_UNSUPPORTED;
+  if (c->kv_format != G4_KV_BF16 && c->kv_format != G4_KV_INT8) return G4_ERR_INVALID_ARG;
+  if (c->kv_page_size < 0 || c->kv_pages < 0) return G4_ERR_INVALID_ARG;
+  if (c->kv_page_size > 0 && (c->kv_page_size < 16 || (c->kv_page_size & (c->kv_page_size - 1))))
+    return G4_ERR_UNSUPPORTED;  // pages of a power of two >= 16 positions
+  if (c->table_format != G4_BF16 && c->table_format != G4_W4A16) return G4_ERR_INVALID_ARG;
   return G4_OK;
 }
 
@@ -1700,6 +1743,7 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   if (!h->embed || !h->ple_table || !h->g_ppn || !h->g_final || !w->layers || !w->ple_model_proj.w)
     return G4_ERR_INVALID_ARG;
   if (fmt == G4_W4A16 && !w->ple_model_proj.scales) return G4_ERR_INVALID_ARG;
+  if (c.table_format == G4_W4A16) return G4_ERR_UNSUPPORTED;
 
   // layer schedule: type, share source, ownership ("One TPU chip, eight agents", The engine)
   std::vector<int> full(L), src(L);
@@ -1755,17 +1799,43 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   TRY(build_lin(h, G4_BF16, H, {{w->embed, nullptr, c.vocab}}, false, &h->lm, st, keep));
   plan_lin(h->lm, h->sms, true);
 
-  // KV cache: owning layers only; [max_batch][max_context][d] bf16 each for K and V.
+  // KV cache: owning layers only.  Static: [max_batch][max_context] rows of d values for K
+  // and for V.  Paged: a pool of n_pages pages of page_size rows, and one page table.
+  h->kv8 = c.kv_format == G4_KV_INT8;
+  size_t kv_rows = (size_t)c.max_batch * c.max_context;
+  if (c.kv_page_size > 0) {
+    while ((1 << h->page_shift) < c.kv_page_size) ++h->page_shift;
+    h->max_pages = cdiv(c.max_context, c.kv_page_size);
+    h->n_pages = c.kv_pages > 0 ? c.kv_pages : c.max_batch * h->max_pages;
+    kv_rows = (size_t)h->n_pages << h->page_shift;
+    h->pt_host.assign((size_t)c.max_batch * h->max_pages, -1);
+    h->slot_pages.assign(c.max_batch, 0);
+    for (int pg = h->n_pages - 1; pg >= 0; --pg) h->free_pages.push_back(pg);  // page 0 taken first
+    TRY(dalloc(h, &h->page_table, h->pt_host.size()));
+    CK(cudaMemcpyAsync(h->page_table, h->pt_host.data(), h->pt_host.size() * sizeof(int), cudaMemcpyHostToDevice, st));
+    CK(cudaStreamSynchronize(st));
+  }
   h->kc.resize(n_own);
   h->vc.resize(n_own);
+  h->ksc.assign(n_own, nullptr);
+  h->vsc.assign(n_own, nullptr);
   for (int l = 0; l < L; ++l) {
     const Layer& Y = h->layers[l];
     if (!Y.own) continue;
-    const size_t n = (size_t)c.max_batch * c.max_context * Y.d;
-    TRY(dalloc(h, &h->kc[Y.kv], n));
-    TRY(dalloc(h, &h->vc[Y.kv], n));
-    CK(cudaMemsetAsync(h->kc[Y.kv], 0, n * 2, st));
-    CK(cudaMemsetAsync(h->vc[Y.kv], 0, n * 2, st));
+    const size_t nb = kv_rows * Y.d * (h->kv8 ? 1 : 2);
+    uint8_t *kb = nullptr, *vb = nullptr;
+    TRY(dalloc(h, &kb, nb));
+    TRY(dalloc(h, &vb, nb));
+    CK(cudaMemsetAsync(kb, 0, nb, st));
+    CK(cudaMemsetAsync(vb, 0, nb, st));
+    h->kc[Y.kv] = kb;
+    h->vc[Y.kv] = vb;
+    if (h->kv8) {
+      TRY(dalloc(h, &h->ksc[Y.kv], kv_rows));
+      TRY(dalloc(h, &h->vsc[Y.kv], kv_rows));
+      CK(cudaMemsetAsync(h->ksc[Y.kv], 0, kv_rows * 4, st));
+      CK(cudaMemsetAsync(h->vsc[Y.kv], 0, kv_rows * 4, st));
+    }
   }
   // RoPE tables (fp64 angles, rounded to fp32)
   for (int t = 0; t < 2; ++t) {
@@ -1945,6 +2015,36 @@ void g4_free(g4_handle* h) {
 
 int64_t g4_device_bytes(const g4_handle* h) { return h ? (int64_t)h->bytes : 0; }
 
+g4_status g4_kv_reserve(g4_handle* h, g4_stream stream, int32_t slot, int32_t n_positions) {
+  if (!h || slot < 0 || slot >= h->cfg.max_batch || n_positions < 0) return G4_ERR_INVALID_ARG;
+  if (n_positions > h->cfg.max_context) return G4_ERR_CONTEXT_OVERFLOW;
+  if (!h->page_table) return G4_OK;
+  DEVICE_GUARD(h->device);
+  return kv_reserve_impl(h, reinterpret_cast<cudaStream_t>(stream), slot, n_positions);
+}
+
+g4_status g4_kv_release(g4_handle* h, g4_stream stream, int32_t slot) {
+  if (!h || slot < 0 || slot >= h->cfg.max_batch) return G4_ERR_INVALID_ARG;
+  if (!h->page_table) return G4_OK;
+  DEVICE_GUARD(h->device);
+  int& have = h->slot_pages[slot];
+  if (have == 0) return G4_OK;
+  int* row = h->pt_host.data() + (size_t)slot * h->max_pages;
+  for (int k = have - 1; k >= 0; --k) {
+    h->free_pages.push_back(row[k]);
+    row[k] = -1;
+  }
+  CK(cudaMemcpyAsync(h->page_table + (size_t)slot * h->max_pages, row, have * sizeof(int), cudaMemcpyHostToDevice,
+                     reinterpret_cast<cudaStream_t>(stream)));
+  have = 0;
+  return G4_OK;
+}
+
+int32_t g4_kv_pages_free(const g4_handle* h) {
+  if (!h || !h->page_table) return -1;
+  return (int32_t)h->free_pages.size();
+}
+
 int32_t g4_step_mode(const g4_handle* h, int32_t n_seq) {
   if (!h) return -1;
   return (h->mega_ok && h->mega_on && n_seq <= 2) ? 1 : 0;
@@ -2017,6 +2117,13 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
   }
   DEVICE_GUARD(h->device);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (h->page_table) {  // pages for every prompt position, all or none
+    long extra = 0;
+    for (int i = 0; i < n_seq; ++i)
+      extra += std::max(0, cdiv(start_pos[i] + len[i], 1 << h->page_shift) - h->slot_pages[slots[i]]);
+    if (extra > (long)h->free_pages.size()) return G4_ERR_OOM;
+    for (int i = 0; i < n_seq; ++i) TRY(kv_reserve_impl(h, st, slots[i], start_pos[i] + len[i]));
+  }
   auto upload = [&](const std::vector<int>& host) -> g4_status {
     if (h->pf_cap < host.size()) {
       if (h->pf_buf) { CK(cudaStreamSynchronize(st)); cudaFree(h->pf_buf); h->pf_buf = nullptr; h->pf_cap = 0; }

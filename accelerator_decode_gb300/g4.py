@@ -21,6 +21,8 @@ G4_ERR_TIMEOUT = -6
 G4_ERR_DEVICE_CHECK = -7
 G4_BF16 = 0
 G4_W4A16 = 1
+G4_KV_BF16 = 0
+G4_KV_INT8 = 1
 G4_DEV_BAD_TOKEN = 1
 G4_DEV_BAD_POSITION = 2
 G4_DEV_TIMEOUT = 4
@@ -32,13 +34,15 @@ _INT_FIELDS = ("num_layers", "num_kv_shared_layers", "hidden", "num_q_heads", "n
                "group_size")
 _FLOAT_FIELDS = ("rms_eps", "rope_theta_sliding", "rope_theta_full", "attn_scale_sliding",
                  "attn_scale_full")
+_TAIL_FIELDS = ("kv_format", "kv_page_size", "kv_pages", "table_format")
 LINEAR_NAMES = ("q", "k", "v", "o", "gate", "up", "down", "ple_gate", "ple_proj")
 NORM_NAMES = ("in_norm", "post_attn_norm", "pre_ffw_norm", "post_ffw_norm", "post_ple_norm",
               "q_norm", "k_norm")
 
 
 class g4_config(ctypes.Structure):
-    _fields_ = [(n, c_int32) for n in _INT_FIELDS] + [(n, c_float) for n in _FLOAT_FIELDS]
+    _fields_ = ([(n, c_int32) for n in _INT_FIELDS] + [(n, c_float) for n in _FLOAT_FIELDS]
+                + [(n, c_int32) for n in _TAIL_FIELDS])
 
 
 class g4_linear(ctypes.Structure):
@@ -53,7 +57,8 @@ class g4_layer_weights(ctypes.Structure):
 class g4_weights(ctypes.Structure):
     _fields_ = [("embed", c_void_p), ("ple_table", c_void_p), ("ple_model_proj", g4_linear),
                 ("ple_proj_norm", c_void_p), ("final_norm", c_void_p),
-                ("layers", POINTER(g4_layer_weights))]
+                ("layers", POINTER(g4_layer_weights)), ("embed_scales", c_void_p),
+                ("ple_table_scales", c_void_p)]
 
 
 class g4_phase_stat(ctypes.Structure):
@@ -90,6 +95,9 @@ def _load():
         "g4_profile_step": (c_int, [P, P, c_int32, P, P, P, P, P, c_int32, POINTER(g4_phase_stat), c_int32,
                                     POINTER(c_int32)]),
         "g4_free": (None, [P]),
+        "g4_kv_reserve": (c_int, [P, P, c_int32, c_int32]),
+        "g4_kv_release": (c_int, [P, P, c_int32]),
+        "g4_kv_pages_free": (c_int32, [P]),
         "g4_status_string": (ctypes.c_char_p, [c_int]),
         "g4_last_cuda_error": (ctypes.c_char_p, []),
         "g4_linear_create": (c_int, [c_int, c_int32, c_int32, c_int32, P, P, POINTER(P)]),
@@ -121,8 +129,13 @@ def check(status, where):
         raise G4Error(status, where)
 
 
-def make_config(cfg, weight_format, max_batch, max_context):
+def make_config(cfg, weight_format, max_batch, max_context, kv_format="bf16", kv_page_size=0, kv_pages=0,
+                table_format="bf16"):
     c = g4_config()
+    c.kv_format = G4_KV_INT8 if kv_format == "int8" else G4_KV_BF16
+    c.kv_page_size = int(kv_page_size)
+    c.kv_pages = int(kv_pages)
+    c.table_format = G4_W4A16 if table_format == "w4a16" else G4_BF16
     for n in _INT_FIELDS:
         if n == "weight_format":
             c.weight_format = G4_W4A16 if weight_format == "w4a16" else G4_BF16
@@ -179,6 +192,18 @@ def g4_profile_step(h, stream, n_seq, d_slots, d_tokens, d_positions, d_next_ids
                               arr, 64, ctypes.byref(n)), "g4_profile_step")
     return [dict(name=arr[i].name.decode(), launches=arr[i].launches, ms_total=arr[i].ms_total,
                  bytes_total=arr[i].bytes_total) for i in range(n.value)]
+
+
+def g4_kv_reserve(h, stream, slot, n_positions):
+    check(lib.g4_kv_reserve(h, stream, slot, n_positions), "g4_kv_reserve")
+
+
+def g4_kv_release(h, stream, slot):
+    check(lib.g4_kv_release(h, stream, slot), "g4_kv_release")
+
+
+def g4_kv_pages_free(h):
+    return lib.g4_kv_pages_free(h)
 
 
 def g4_free(h):

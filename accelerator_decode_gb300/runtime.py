@@ -28,17 +28,23 @@ def stream_handle(stream=None):
 
 
 class Decoder:
-    """One libg4 handle.  `weights` is a host weight dict in the canonical format (synth)."""
+    """One libg4 handle.  `weights` is a host weight dict in the canonical format (synth).
+    kv_format "bf16" or "int8" (cache rows); kv_page_size 0 (static rows) or a power of two
+    (paged cache of kv_pages pages, 0 = as many as static rows would take).  Vocabulary
+    tables given as int4 dicts (packed, scales) select the int4 table format."""
 
-    def __init__(self, cfg, weights, max_batch, max_context, device=0):
-        if isinstance(weights["embed"], dict) or isinstance(weights["ple_table"], dict):
-            raise ValueError("g4_create takes bf16 vocabulary tables (token embedding and "
-                             "per-layer table); int4 tables are not supported by the library")
+    def __init__(self, cfg, weights, max_batch, max_context, device=0, kv_format="bf16", kv_page_size=0,
+                 kv_pages=0):
+        t4 = [isinstance(weights[k], dict) for k in ("embed", "ple_table")]
+        if t4[0] != t4[1]:
+            raise ValueError("the token embedding and the per-layer table share one table format")
         self.cfg = cfg
         self.device = torch.device("cuda", device)
         self.max_batch, self.max_context = max_batch, max_context
         self.fmt = weights["fmt"]
-        self.c = _g4.make_config(cfg, self.fmt, max_batch, max_context)
+        self.table_format = "w4a16" if t4[0] else "bf16"
+        self.c = _g4.make_config(cfg, self.fmt, max_batch, max_context, kv_format, kv_page_size, kv_pages,
+                                 self.table_format)
         keep, tmp = [], []
 
         def borrow(a):
@@ -68,8 +74,14 @@ class Decoder:
                 setattr(layers[l], n, borrow(lw[n]))
             layers[l].layer_scale = float(lw["layer_scale"])
         w = _g4.g4_weights()
-        w.embed = borrow(weights["embed"])
-        w.ple_table = borrow(weights["ple_table"])
+        if self.table_format == "w4a16":
+            w.embed = borrow(weights["embed"]["packed"])
+            w.embed_scales = borrow(weights["embed"]["scales"])
+            w.ple_table = borrow(weights["ple_table"]["packed"])
+            w.ple_table_scales = borrow(weights["ple_table"]["scales"])
+        else:
+            w.embed = borrow(weights["embed"])
+            w.ple_table = borrow(weights["ple_table"])
         w.ple_model_proj = linear(weights["ple_model_proj"])
         w.ple_proj_norm = borrow(weights["ple_proj_norm"])
         w.final_norm = borrow(weights["final_norm"])
@@ -105,6 +117,17 @@ class Decoder:
     def profile_step(self, d_slots, d_tokens, d_positions, d_next, d_logits=None, repeats=1, stream=None):
         return _g4.g4_profile_step(self.h, stream_handle(stream), d_tokens.numel(), _ptr(d_slots), _ptr(d_tokens),
                                    _ptr(d_positions), _ptr(d_next), _ptr(d_logits), repeats)
+
+    def reserve(self, slot, n_positions, stream=None):
+        """Paged cache: pages for positions [0, n_positions) of `slot` (no-op when static)."""
+        _g4.g4_kv_reserve(self.h, stream_handle(stream), int(slot), int(n_positions))
+
+    def release(self, slot, stream=None):
+        """Paged cache: return the slot's pages to the pool."""
+        _g4.g4_kv_release(self.h, stream_handle(stream), int(slot))
+
+    def pages_free(self):
+        return _g4.g4_kv_pages_free(self.h)
 
     def device_error(self, stream=None):
         return _g4.g4_get_device_error(self.h, stream_handle(stream))

@@ -50,6 +50,9 @@ typedef enum g4_status {
 } g4_status;
 
 enum { G4_BF16 = 0, G4_W4A16 = 1 };
+/* KV cache row formats: bf16 values, or int8 codes with one fp32 scale per row ("One TPU
+ * chip, eight agents", Measured: the raw JAX decode kernel, int8 KV cache). */
+enum { G4_KV_BF16 = 0, G4_KV_INT8 = 1 };
 
 /* Device error word bits (g4_get_device_error). */
 enum { G4_DEV_BAD_TOKEN = 1, G4_DEV_BAD_POSITION = 2, G4_DEV_TIMEOUT = 4, G4_DEV_BAD_SLOT = 8 };
@@ -71,6 +74,17 @@ typedef struct g4_config {
   int32_t group_size;    /* 32 */
   float rms_eps, rope_theta_sliding, rope_theta_full;
   float attn_scale_sliding, attn_scale_full; /* 0 => 1/sqrt(head_dim) */
+  /* KV cache.  kv_format: G4_KV_BF16 or G4_KV_INT8 (row r of d values -> a = max|r|,
+   * s = a / 127, c = round-half-even(r / s) clipped to +-127, stored value c * s).
+   * kv_page_size: 0 = static rows (slot, position); else paged ("Six serving engines on one
+   * Cloud TPU v5e chip", Step 3: page size 128), a power of two >= 16: a slot's positions
+   * [k * page, (k+1) * page) live in the pool page its page table names (g4_kv_reserve).
+   * kv_pages: pool pages (0 = max_batch * ceil(max_context / kv_page_size)). */
+  int32_t kv_format, kv_page_size, kv_pages;
+  /* Vocabulary tables (embed / lm_head and ple_table): G4_BF16, or G4_W4A16 with the
+   * linears' int4 layout and bf16 scales per 32 columns ("Six serving engines on one Cloud
+   * TPU v5e chip", What Changes and What Stays: int4 embedding tables). */
+  int32_t table_format;
 } g4_config;
 
 /* One projection y = W x, W [N, K].
@@ -97,7 +111,9 @@ typedef struct g4_layer_weights {
 
 /* Whole-model tensors.  embed: bf16 [vocab, hidden], also the tied lm_head.
  * ple_table: bf16 [vocab, num_layers * ple_dim].  ple_model_proj: [num_layers*ple_dim, hidden].
- * layers: HOST array of num_layers entries. */
+ * layers: HOST array of num_layers entries.  With table_format G4_W4A16, embed and ple_table
+ * are int32 [rows, cols/8] in the linears' int4 layout and embed_scales / ple_table_scales
+ * bf16 [rows, cols/32]; the dequantised value is bf16(q * scale). */
 typedef struct g4_weights {
   const void* embed;
   const void* ple_table;
@@ -105,6 +121,8 @@ typedef struct g4_weights {
   const void* ple_proj_norm; /* bf16 [ple_dim] */
   const void* final_norm;    /* bf16 [hidden] */
   const g4_layer_weights* layers;
+  const void* embed_scales;     /* table_format G4_W4A16 only */
+  const void* ple_table_scales; /* table_format G4_W4A16 only */
 } g4_weights;
 
 typedef struct g4_handle g4_handle;
@@ -146,6 +164,23 @@ g4_status g4_prefill(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_
 g4_status g4_decode_step(g4_handle* h, g4_stream stream, int32_t n_seq, const int32_t* d_slots,
                          const int32_t* d_tokens, const int32_t* d_positions,
                          int32_t* d_next_ids, float* d_logits);
+
+/* Paged KV cache (kv_page_size > 0): make cache slot `slot` hold positions [0,
+ * n_positions), taking pool pages as needed and writing the slot's page-table entries on
+ * `stream` (host arrays are not touched after return).  Pages already held stay; none is
+ * taken when the pool is short.  A decode step whose position has no page sets
+ * G4_DEV_BAD_POSITION and leaves that row's K/V unwritten.  g4_prefill reserves its own
+ * positions.  With static rows (kv_page_size == 0) this only checks n_positions.
+ * Errors: G4_ERR_INVALID_ARG (slot out of range, n_positions < 0), G4_ERR_CONTEXT_OVERFLOW
+ * (n_positions > max_context), G4_ERR_OOM (not enough free pages). */
+g4_status g4_kv_reserve(g4_handle* h, g4_stream stream, int32_t slot, int32_t n_positions);
+
+/* Paged KV cache: return every page of `slot` to the pool (its positions become unheld).
+ * No-op with static rows.  Errors: G4_ERR_INVALID_ARG. */
+g4_status g4_kv_release(g4_handle* h, g4_stream stream, int32_t slot);
+
+/* Free pool pages (paged KV cache), or -1 with static rows or a NULL handle. */
+int32_t g4_kv_pages_free(const g4_handle* h);
 
 /* Synchronise `stream`, read and clear the device error word.  *word_out (nullable) gets
  * the G4_DEV_* bits.  Returns G4_ERR_TIMEOUT if the timeout bit is set, else

@@ -46,14 +46,16 @@ def test_status_strings(g4):
 def test_struct_layout_matches_c(g4, tmp_path):
     src = tmp_path / "sz.c"
     src.write_text('#include "g4.h"\n#include <stdio.h>\n#include <stddef.h>\n'
-                   'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(g4_config), '
+                   'int main(void){printf("%zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(g4_config), '
                    'sizeof(g4_linear), sizeof(g4_layer_weights), sizeof(g4_weights), '
-                   'offsetof(g4_config, rms_eps), offsetof(g4_layer_weights, layer_scale));return 0;}\n')
+                   'offsetof(g4_config, rms_eps), offsetof(g4_layer_weights, layer_scale), '
+                   'offsetof(g4_config, table_format), offsetof(g4_weights, ple_table_scales));return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = list(map(int, subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()))
     want = [ctypes.sizeof(g4.g4_config), ctypes.sizeof(g4.g4_linear), ctypes.sizeof(g4.g4_layer_weights),
-            ctypes.sizeof(g4.g4_weights), g4.g4_config.rms_eps.offset, g4.g4_layer_weights.layer_scale.offset]
+            ctypes.sizeof(g4.g4_weights), g4.g4_config.rms_eps.offset, g4.g4_layer_weights.layer_scale.offset,
+            g4.g4_config.table_format.offset, g4.g4_weights.ple_table_scales.offset]
     assert got == want
 
 
