@@ -119,6 +119,11 @@ struct g4_handle {
   std::vector<Layer> layers;
   Lin pmp, lm;
   const __nv_bfloat16 *embed = nullptr, *ple_table = nullptr, *g_ppn = nullptr, *g_final = nullptr;
+  // int4 vocabulary tables (table_format G4_W4A16): borrowed words and scales; the lm_head
+  // is then an int4 projection built from the embedding's
+  bool t4 = false;
+  const uint32_t *embed_q = nullptr, *ple_q = nullptr;
+  const __nv_bfloat16 *embed_s = nullptr, *ple_s = nullptr;
   // KV cache per owning layer: rows of d values (bf16, or int8 codes with an fp32 scale per
   // row in ksc / vsc).  Static rows: slot * max_context + position.  Paged: a pool of n_pages
   // pages of 2^page_shift rows per layer, one page table for all layers (device copy
@@ -399,6 +404,7 @@ int init_kernel_attrs(int device) {
   attrs_gemv<FMT_W4A16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_PLE>(optin);
   attrs_gemv<FMT_BF16, 1, EPI_ARGMAX>(optin);
+  attrs_gemv<FMT_W4A16, 1, EPI_ARGMAX>(optin);
   attrs_staged<FMT_W4A16>(optin);
   attrs_staged<FMT_BF16>(optin);
   set_max_dyn(gemm_tc_kernel, optin);
@@ -770,7 +776,8 @@ void run_gemv(const Lin& L, int epi, const GemvIO& io, int n, float eps, const S
         else launch_fmt<FMT_BF16, 1, EPI_PLE>(a, nb, grid, st);
         break;
       case EPI_ARGMAX:
-        launch_fmt<FMT_BF16, 1, EPI_ARGMAX>(a, nb, grid, st);
+        if (w4) launch_fmt<FMT_W4A16, 1, EPI_ARGMAX>(a, nb, grid, st);
+        else launch_fmt<FMT_BF16, 1, EPI_ARGMAX>(a, nb, grid, st);
         break;
     }
   }
@@ -865,6 +872,15 @@ g4_status run_step_mega(g4_handle* h, cudaStream_t st, int n, const int* d_slots
 // first layer after which no layer writes K/V on, only rows keep_idx[0 .. n_keep) (their
 // slots and positions in keep_slots / keep_pos) go on: a prompt row that ends no sequence
 // feeds nothing past its last K/V write.  n_keep == 0 ends the step there.
+// int4 vocabulary tables in the embedding gather's arguments.
+void set_tables(const g4_handle* h, EmbedArgs& ea) {
+  ea.t4 = h->t4;
+  ea.embed_q = h->embed_q;
+  ea.embed_s = h->embed_s;
+  ea.ple_q = h->ple_q;
+  ea.ple_s = h->ple_s;
+  ea.ple_group = h->cfg.ple_dim;
+}
 // Cache of layer Src (its K/V rows, scales and page table) in attention arguments.
 void kv_args(const g4_handle* h, const Layer& Src, AttnArgs& a) {
   a.kc = h->kc[Src.kv];
@@ -936,6 +952,7 @@ g4_status run_step_staged(g4_handle* h, cudaStream_t st, int n, const int* d_slo
 
   EmbedArgs ea{d_tokens, d_idx, h->embed, h->ple_table, c.vocab, H, LP,
                (float)std::sqrt((double)H), (float)std::sqrt((double)P), h->x0, h->tok, h->err};
+  set_tables(h, ea);
   {
     ProfScope ps(prof, "embed", (double)n * (H + LP) * 2);
     launch(embed_kernel, dim3(cdiv(H + LP, 8 * 256), n), dim3(256), 0, st, ea);
@@ -1101,6 +1118,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
 
   EmbedArgs ea{d_tokens, d_idx, h->embed, h->ple_table, c.vocab, H, LP,
                (float)std::sqrt((double)H), (float)std::sqrt((double)P), h->x0, h->tok, h->err};
+  set_tables(h, ea);
   {
     ProfScope ps(prof, "embed", (double)n * (H + LP) * 2);
     launch(embed_kernel, dim3(cdiv(H + LP, 8 * 256), n), dim3(256), 0, st, ea);
@@ -1359,7 +1377,7 @@ g4_status build_mega(g4_handle* h, cudaStream_t st) {
   const g4_config& c = h->cfg;
   const int H = c.hidden, L = c.num_layers, P = c.ple_dim, nq = c.num_q_heads;
   const int G = h->sms, NB = 2;
-  if (H % 8 || h->kv8) return G4_OK;  // the persistent step reads bf16 cache rows only
+  if (H % 8 || h->kv8 || h->t4) return G4_OK;  // the persistent step: bf16 cache rows and tables only
   std::vector<MegaPhase> prog;
   size_t smem_f = 64;  // floats
   auto wred_f = [&]() { return (size_t)2 * kMegaWarps * 2 * NB * 32; };  // double-buffered warp partials
@@ -1743,7 +1761,14 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   if (!h->embed || !h->ple_table || !h->g_ppn || !h->g_final || !w->layers || !w->ple_model_proj.w)
     return G4_ERR_INVALID_ARG;
   if (fmt == G4_W4A16 && !w->ple_model_proj.scales) return G4_ERR_INVALID_ARG;
-  if (c.table_format == G4_W4A16) return G4_ERR_UNSUPPORTED;
+  if (c.table_format == G4_W4A16) {
+    if (!w->embed_scales || !w->ple_table_scales) return G4_ERR_INVALID_ARG;
+    h->t4 = true;
+    h->embed_q = static_cast<const uint32_t*>(w->embed);
+    h->embed_s = static_cast<const __nv_bfloat16*>(w->embed_scales);
+    h->ple_q = static_cast<const uint32_t*>(w->ple_table);
+    h->ple_s = static_cast<const __nv_bfloat16*>(w->ple_table_scales);
+  }
 
   // layer schedule: type, share source, ownership ("One TPU chip, eight agents", The engine)
   std::vector<int> full(L), src(L);
@@ -1796,7 +1821,10 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
   }
   TRY(build_lin(h, fmt, H, {{w->ple_model_proj.w, w->ple_model_proj.scales, L * P}}, false, &h->pmp, st, keep));
   plan_lin(h->pmp, h->sms, false);
-  TRY(build_lin(h, G4_BF16, H, {{w->embed, nullptr, c.vocab}}, false, &h->lm, st, keep));
+  if (h->t4)
+    TRY(build_lin(h, G4_W4A16, H, {{w->embed, w->embed_scales, c.vocab}}, false, &h->lm, st, keep));
+  else
+    TRY(build_lin(h, G4_BF16, H, {{w->embed, nullptr, c.vocab}}, false, &h->lm, st, keep));
   plan_lin(h->lm, h->sms, true);
 
   // KV cache: owning layers only.  Static: [max_batch][max_context] rows of d values for K

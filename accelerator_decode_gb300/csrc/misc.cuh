@@ -7,16 +7,26 @@ namespace g4 {
 // x0[b] = E[t_b] * sqrt(H);  tok[b] = T_ple[t_b] * sqrt(P)   (fp32)
 // Token ids come from tokens[b] or, with idx != nullptr, tokens[idx[b]].
 // "Porting Gemma 4 E2B to SGLang-JAX", Step 3: tok = embed_tokens_per_layer(ids) * ple_dim**0.5.
+// int4 tables ("Six serving engines on one Cloud TPU v5e chip", What Changes and What Stays):
+// rows of packed int32 words (8 signed nibbles, low first) with a bf16 scale per `group`
+// values; a table value is bf16(q * s) as for the int4 linears.
 struct EmbedArgs {
   const int* tokens;
   const int* idx;
-  const __nv_bfloat16* embed;      // [V][H]
+  const __nv_bfloat16* embed;      // [V][H] (bf16 tables)
   const __nv_bfloat16* ple_table;  // [V][LP]
   int V, H, LP;
   float sqrt_h, sqrt_p;
   float* x0;   // [nb][H]
   float* tok;  // [nb][LP]
   int* err;
+  // int4 tables (t4): words [V][H/8] / [V][LP/8], scales [V][H/32] / [V][LP/ple_group]
+  int t4;
+  const uint32_t* embed_q;
+  const __nv_bfloat16* embed_s;
+  const uint32_t* ple_q;
+  const __nv_bfloat16* ple_s;
+  int ple_group;
 };
 
 // Grid (ceil((H + LP) / (8 * blockDim.x)), nb): each thread converts 8 bf16 (one 16-byte load).
@@ -42,6 +52,22 @@ __global__ void embed_kernel(const EmbedArgs a) {
     dst = a.tok + (size_t)b * a.LP + (i8 - a.H);
     sc = a.sqrt_p;
   } else {
+    return;
+  }
+  if (a.t4) {  // one word of 8 nibbles; a scale group holds whole words
+    const bool e = i8 < a.H;
+    const int k = e ? i8 : i8 - a.H;
+    const uint32_t w = e ? a.embed_q[(size_t)t * (a.H / 8) + k / 8] : a.ple_q[(size_t)t * (a.LP / 8) + k / 8];
+    const float s = e ? bf16f(a.embed_s[(size_t)t * (a.H / 32) + k / 32])
+                      : bf16f(a.ple_s[(size_t)t * (a.LP / a.ple_group) + k / a.ple_group]);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = (int)((w >> (4 * j)) & 0xFu) - (((w >> (4 * j)) & 0x8u) ? 16 : 0);
+      v[j] = bf16f(__float2bfloat16_rn((float)q * s)) * sc;  // q * s is exact in fp32
+    }
+    reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
     return;
   }
   const uint4 u = *reinterpret_cast<const uint4*>(src);

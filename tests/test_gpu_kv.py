@@ -201,3 +201,35 @@ def test_paged_pool_limits(rt):
     dec.decode_step(slots, tok, torch.tensor([8], dtype=torch.int32, device="cuda"), out)
     assert dec.device_error()[1] == 0
     dec.close()
+
+
+# ---------------------------------------------------------------------------------------------
+# int4 vocabulary tables ("Six serving engines on one Cloud TPU v5e chip", What Changes and
+# What Stays): the token embedding, the per-layer table and the tied lm_head in int4.
+@pytest.mark.parametrize("name,fmt,batch", [("tiny", "bf16", 2), ("tiny10", "w4a16", 2), ("tiny10", "w4a16", 8)])
+def test_int4_tables_match_oracle(rt, name, fmt, batch):
+    """batch 8 puts the lm_head on the tensor-core GEMM; 2 on the GEMV."""
+    cfg = synth.get_config(name)
+    w = synth.make_weights(cfg, fmt, seed=13, gain_std=0.1, tables="int4")
+    prompts = synth.make_prompts(cfg["vocab"], batch, 12, seed=30)
+    ref = oracle.Oracle(cfg, w, max_batch=batch, max_context=64).generate(prompts, 14, keep_logits=True)
+    dec = rt.Decoder(cfg, w, max_batch=batch, max_context=64)
+    assert dec.table_format == "w4a16"
+    toks, logits = forced(dec, list(prompts), ref)
+    assert dec.device_error()[1] == 0
+    dec.close()
+    check(ref, toks, logits, f"int4 tables {name}/{fmt}/b{batch}")
+
+
+def test_all_variants_together_e2b_heads(rt):
+    """int4 tables, int8 cache rows and a paged cache at once, E2B head dims, 300 tokens."""
+    cfg = synth.get_config("mid")
+    w = synth.make_weights(cfg, "w4a16", seed=17, gain_std=0.1, tables="int4")
+    prompts = synth.make_prompts(cfg["vocab"], 2, 300, seed=31)
+    ref = oracle.Oracle(cfg, w, max_batch=2, max_context=384, kv_dtype="int8").generate(
+        prompts, 6, keep_logits=True)
+    dec = rt.Decoder(cfg, w, max_batch=2, max_context=384, kv_format="int8", kv_page_size=128)
+    toks, logits = forced(dec, list(prompts), ref, paged=True)
+    assert dec.device_error()[1] == 0
+    dec.close()
+    check(ref, toks, logits, "int4 tables + int8 paged")
