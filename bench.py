@@ -6,7 +6,10 @@
 A step is one greedy decode step of the whole model (embedding, per-layer embeddings, all
 projections, attention with KV sharing, norms, lm_head and argmax) for the workload's batch.
 Default workload: the E2B-shaped W4A16 model at batch 1 after a 128-token prompt, timed over
-the 511 decode steps that produce tokens 2..512 (positions 128..638).
+the 511 decode steps that produce tokens 2..512 (positions 128..638): one untimed run, then
+three timed runs of K steps from the same start; the headline is their median (IQR beside
+it).  Companion figures in the same line: batch 64, bf16 at batch 1 and 64, and the model
+with int4 vocabulary tables and int8 cache rows.
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs an independent replica on its
 own GPU (the path has no exchange step); value = tokens of all ranks / max rank time.
@@ -30,6 +33,7 @@ import synth  # noqa: E402
 
 METRIC = "decode tok/s at batch 1 & 64, E2B-shaped bf16/W4A16; % of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
+RUNS = 3  # timed runs after the untimed one; the headline is their median
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -72,13 +76,13 @@ def _owning(cfg):
     return [l < first or not any(full[j] == full[l] for j in range(first)) for l in range(L)]
 
 
-def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False):
+def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False, tables="bf16", kv="bf16"):
     """Unique bytes one decode step must move: every weight once (int4 at 0.5 B + a bf16 scale
-    per 32, or bf16), the tied bf16 lm_head, and per sequence the visible K/V of the owning
-    layers' caches (read once even when aliased), the new K/V row, the per-layer-embedding row
-    and the embedding row.  count_aliased also counts each KV-sharing layer's read of its
-    source cache (the bytes the attention kernels actually request).  Returns (weight bytes,
-    mean KV+row bytes per step over positions)."""
+    per 32, or bf16), the tied lm_head (bf16, or int4 tables), and per sequence the visible K/V
+    of the owning layers' caches (read once even when aliased; int8 rows add a 4-byte scale),
+    the new K/V row, the per-layer-embedding row and the embedding row.  count_aliased also
+    counts each KV-sharing layer's read of its source cache (the bytes the attention kernels
+    actually request).  Returns (weight bytes, mean KV+row bytes per step over positions)."""
     H, P, V, L = cfg["hidden"], cfg["ple_dim"], cfg["vocab"], cfg["num_layers"]
     own = _owning(cfg)
     n_lin = L * P * H
@@ -89,7 +93,9 @@ def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False):
                 continue
             n_lin += n * k
     per_w = 0.5 + 2.0 / 32 if fmt == "w4a16" else 2.0
-    wbytes = n_lin * per_w + V * H * 2
+    t4 = tables == "int4"
+    wbytes = n_lin * per_w + (V * H * (0.5 + 2.0 / 32) if t4 else V * H * 2)
+    row = (lambda d: d + 4) if kv == "int8" else (lambda d: 2 * d)   # bytes of one cache row
     kv = []
     for p in positions:
         T = p + 1
@@ -100,8 +106,8 @@ def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False):
             full = synth.layer_is_full(cfg, l)
             d = cfg["head_dim_full"] if full else cfg["head_dim_sliding"]
             keys = T if full else min(T, cfg["sliding_window"])
-            b += keys * d * 2 * 2 + (d * 2 * 2 if own[l] else 0)
-        b += L * P * 2 + H * 2
+            b += keys * row(d) * 2 + (row(d) * 2 if own[l] else 0)
+        b += (L * P * 0.5 + L * 2 + H * 0.5 + H / 32 * 2) if t4 else (L * P * 2 + H * 2)
         kv.append(b * batch)
     return wbytes, float(np.mean(kv))
 
@@ -109,7 +115,7 @@ def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False):
 # DRAM traffic / algorithmic bytes of a kernel, from one ncu capture of its current code;
 # traffic scales with the rows a launch streams.
 # Keyed by (weight format, phase); a kernel changed since its capture has no entry.
-MEASURED_TRAFFIC_RATIO = {("w4a16", "gemv.gate_up"): 10716416 / 10616832}
+MEASURED_TRAFFIC_RATIO = {}
 
 
 def measured_peak():
@@ -187,19 +193,20 @@ def cpu_cores():
     return len(os.sched_getaffinity(0))
 
 
-def oracle_sample(cfg, weights, batch, budget_s, n_max):
-    """Time the CPU oracle's decode steps on this host: up to n_max steps or budget_s seconds
-    of work, from position 0 of seeded prompts.  Returns (tok/s, steps, seconds, batch used)."""
+def oracle_sample(cfg, weights, batch, budget_s, n_max, start=128):
+    """Time the CPU oracle's decode steps on this host at the GPU's positions: an untimed
+    teacher-forced prefill of `start` tokens, then up to n_max decode steps (positions start,
+    start + 1, ...) or budget_s seconds of work.  Returns (tok/s, steps, seconds, batch used)."""
     import oracle
     ob = batch
-    o = oracle.Oracle(cfg, weights, max_batch=ob, max_context=max(8, n_max + 1))
-    prompts = synth.make_prompts(cfg["vocab"], ob, n_max + 1, seed=0, stream=99)
+    o = oracle.Oracle(cfg, weights, max_batch=ob, max_context=start + n_max + 1)
+    prompts = synth.make_prompts(cfg["vocab"], ob, start + n_max + 1, seed=0, stream=99)
     slots = np.arange(ob)
-    o.step(slots, prompts[:, 0], np.zeros(ob, np.int64))      # first step (untimed): touches weights
+    o.prefill(slots, prompts[:, :start])                     # untimed
     t0 = time.perf_counter()
     n = 0
-    while n < n_max - 1:
-        o.step(slots, prompts[:, n + 1], np.full(ob, n + 1))
+    while n < n_max:
+        o.step(slots, prompts[:, start + n], np.full(ob, start + n))
         n += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -255,20 +262,22 @@ def run_gpu(args, wl, cfg, fmt):
         clocks = ClockSampler(local)
         clocks.start()
         steps(min(W, 64))               # keep the GPU busy while the sampler starts
-        reset()
-        st.synchronize()
-        barrier(world)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.nvtx.range_push("g4_timed")
-        e0.record(st)
-        steps(K)
-        e1.record(st)
-        torch.cuda.nvtx.range_pop()
-        e1.synchronize()
-        barrier(world)
+        # one untimed run (the warm-up above), then RUNS timed runs of K steps from the same
+        # start; the headline is the median run, with the interquartile range beside it
+        runs = []
+        for r in range(RUNS):
+            reset()
+            st.synchronize()
+            barrier(world)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            steps(K)
+            e1.record(st)
+            e1.synchronize()
+            barrier(world)
+            runs.append(max_over_ranks(e0.elapsed_time(e1), world, dev))
         clk = clocks.stop()
-        ms = e0.elapsed_time(e1)
-        ms_max = max_over_ranks(ms, world, dev)
+        ms_max = float(np.median(runs))
         out_tokens = tok[K % 2].cpu().numpy().tolist()
         status, word = dec.device_error(stream=st)
 
@@ -349,6 +358,11 @@ def run_gpu(args, wl, cfg, fmt):
         "steps": K,
         "warmup": W,
         "ms_per_step": round(ms_max / K, 5),
+        "runs": {"timed": RUNS, "untimed": 1, "statistic": "median",
+                 "ms_per_step": [round(r / K, 5) for r in runs],
+                 "iqr_ms_per_step": round(float(np.percentile(runs, 75) - np.percentile(runs, 25)) / K, 5),
+                 "iqr_tok_s": round(float(replica_throughput(world, B, K, np.percentile(runs, 25))
+                                          - replica_throughput(world, B, K, np.percentile(runs, 75))), 2)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -385,51 +399,74 @@ def run_gpu(args, wl, cfg, fmt):
         "weight_gen_s": round(t_gen, 1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, n, dt, ob = oracle_sample(cfg, weights, B, args.cpu_budget, 64)
+        v, n, dt, ob = oracle_sample(cfg, weights, B, args.cpu_budget, 64, start=P0)
         result["cpu_baseline"] = {"value": round(v, 3), "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
-                                  "sample": f"{n} oracle decode steps of batch {ob} at positions 1..{n} "
-                                            f"({dt:.1f} s), same weights"}
+                                  "sample": f"{n} oracle decode steps of batch {ob} at positions {P0}..{P0 + n - 1} "
+                                            f"after an untimed {P0}-token prefill ({dt:.1f} s timed), same weights"}
     dec.close()
     if args.batch64 and B == 1 and world == 1:
-        result["batch64"] = batch64_line(args, cfg, weights, local)
+        result["batch64"] = companion_line(args, cfg, weights, local, 64)
+        if fmt == "w4a16" and args.companions:
+            # the metric's bf16 half, and the int4-table / int8-cache variant of the same model
+            del weights
+            wb = synth.make_model_weights(cfg, "bf16", seed=args.seed)
+            result["bf16_b1"] = companion_line(args, cfg, wb, local, 1)
+            result["bf16_b64"] = companion_line(args, cfg, wb, local, 64)
+            del wb
+            wv = synth.make_model_weights(cfg, "w4a16", seed=args.seed, tables="int4")
+            result["w4a16_int4_tables_int8_kv_b1"] = companion_line(args, cfg, wv, local, 1, kv="int8")
+            result["w4a16_int4_tables_int8_kv_b64"] = companion_line(args, cfg, wv, local, 64, kv="int8")
+            del wv
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return result
 
 
-def batch64_line(args, cfg, weights, local):
-    """Companion figure for the metric's batch-64 half: the same model and weights at 64
-    sequences (128-token prompts), W >= 3 warm-up steps, 64 timed steps with CUDA events on
-    the launching stream; inputs (1.9+ GB of weights per step) exceed L2."""
+def companion_line(args, cfg, weights, local, B, kv="bf16"):
+    """Companion figure of the metric (its batch-64 half, its bf16 half, the int4-table /
+    int8-cache variant): `weights` at B sequences after 128-token prompts, W >= 3 untimed
+    steps, then RUNS timed runs of K = 64 steps from the same start (median and IQR), CUDA
+    events on the launching stream; inputs (1.2+ GB of weights per step) exceed L2."""
     import torch
     from accelerator_decode_gb300.runtime import Decoder
-    B, P0, K, W = 64, 128, 64, max(3, min(args.warmup, 8))
+    P0, K, W = 128, 64, max(3, min(args.warmup, 8))
+    tables = "int4" if isinstance(weights["embed"], dict) else "bf16"
     dev = torch.device("cuda", local)
-    dec = Decoder(cfg, weights, max_batch=B, max_context=((P0 + K + W + 1 + 63) // 64) * 64, device=local)
+    dec = Decoder(cfg, weights, max_batch=B, max_context=((P0 + K + W + 1 + 63) // 64) * 64, device=local,
+                  kv_format=kv)
     prompts = synth.make_prompts(cfg["vocab"], B, P0, seed=args.seed)
     st = torch.cuda.Stream()
+    runs = []
     with torch.cuda.stream(st):
         nxt, _ = dec.prefill(list(range(B)), list(prompts), stream=st)
         slots = torch.arange(B, dtype=torch.int32, device=dev)
         tok = [nxt.clone(), torch.empty_like(nxt)]
         pos = torch.full((B,), P0, dtype=torch.int32, device=dev)
-        for i in range(W + K):
-            if i == W:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                st.synchronize()
-                e0.record(st)
+        for i in range(W):
             dec.decode_step(slots, tok[i % 2], pos, tok[(i + 1) % 2], None, stream=st)
             pos.add_(1)
-        e1.record(st)
-        e1.synchronize()
+        for r in range(RUNS):
+            tok[0].copy_(nxt)
+            pos.fill_(P0)
+            st.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for i in range(K):
+                dec.decode_step(slots, tok[i % 2], pos, tok[(i + 1) % 2], None, stream=st)
+                pos.add_(1)
+            e1.record(st)
+            e1.synchronize()
+            runs.append(e0.elapsed_time(e1) / K)
         status, word = dec.device_error(stream=st)
-    ms = e0.elapsed_time(e1) / K
     dec.close()
-    wbytes, kvbytes = algorithmic_bytes(cfg, weights["fmt"], B, [P0 + W + i for i in range(K)])
+    ms = float(np.median(runs))
+    wbytes, kvbytes = algorithmic_bytes(cfg, weights["fmt"], B, [P0 + i for i in range(K)], tables=tables, kv=kv)
     peak, peak_src = measured_peak()
-    return {"value": round(B / (ms / 1e3), 2), "unit": "tok/s", "ms_per_step": round(ms, 5), "steps": K, "warmup": W,
-            "batch": B, "prompt_tokens": P0,
+    return {"value": round(B / (ms / 1e3), 2), "unit": "tok/s", "ms_per_step": round(ms, 5),
+            "iqr_ms_per_step": round(float(np.percentile(runs, 75) - np.percentile(runs, 25)), 5),
+            "runs_ms_per_step": [round(r, 5) for r in runs], "steps": K, "warmup": W,
+            "batch": B, "prompt_tokens": P0, "weights": weights["fmt"], "tables": tables, "kv_cache": kv,
             "step_roofline": {"bytes_per_step": wbytes + kvbytes, "frac": round((wbytes + kvbytes) / (ms / 1e3) / 1e9 / peak, 4),
                               "peak": peak, "peak_source": peak_src},
             "device_error": word}
@@ -529,7 +566,7 @@ def run_reference(args, wl, cfg, fmt):
     # bounded sample: the whole run (warm-up + steps) must end within a few minutes
     budget = args.ref_budget
     total_steps = args.steps + args.warmup
-    v, n, dt, ob = oracle_sample(cfg, weights, B, budget, total_steps)
+    v, n, dt, ob = oracle_sample(cfg, weights, B, budget, total_steps, start=wl["prompt"])
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -544,9 +581,11 @@ def run_reference(args, wl, cfg, fmt):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl["name"], "weights": fmt, "batch_per_gpu": B},
+        "config": {"workload": wl["name"], "weights": fmt, "batch_per_gpu": B, "prompt_tokens": wl["prompt"],
+                   "decode_positions": [wl["prompt"], wl["prompt"] + n - 1]},
         "cpu_baseline": {"value": round(v, 3), "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"{n} oracle decode steps of batch {ob} from position 1 "
+                         "sample": f"{n} oracle decode steps of batch {ob} at positions {wl['prompt']}.."
+                                   f"{wl['prompt'] + n - 1} after an untimed {wl['prompt']}-token prefill "
                                    f"(bounded to {budget:.0f} s of {total_steps} requested)"},
         "e2e": {"value": round(v, 3), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -567,7 +606,9 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-batch64", dest="batch64", action="store_false",
-                    help="skip the batch-64 companion figure of the batch-1 workload")
+                    help="skip the companion figures (batch 64, bf16, int4 tables + int8 cache)")
+    ap.add_argument("--no-companions", dest="companions", action="store_false",
+                    help="keep the batch-64 figure, skip the bf16 and int4-table / int8-cache ones")
     ap.add_argument("--impl-check-only", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args.warmup < 3:
