@@ -270,9 +270,11 @@ def run_gpu(args, wl, cfg, fmt):
             st.synchronize()
             barrier(world)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.nvtx.range_push("g4_timed")
             e0.record(st)
             steps(K)
             e1.record(st)
+            torch.cuda.nvtx.range_pop()
             e1.synchronize()
             barrier(world)
             runs.append(max_over_ranks(e0.elapsed_time(e1), world, dev))
