@@ -9,7 +9,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB = os.path.join(HERE, "libg4.so")
 SOURCES = [os.path.join(HERE, "csrc", "g4.cu")]
-DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("common.cuh", "gemv.cuh", "gemv_s.cuh", "attn.cuh", "misc.cuh", "gemm_tc.cuh", "mega.cuh")]
+DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("common.cuh", "gemv.cuh", "gemv_s.cuh", "attn.cuh", "attn_mqa.cuh", "misc.cuh", "gemm_tc.cuh", "mega.cuh")]
 DEPS.append(os.path.join(os.path.dirname(HERE), "include", "g4.h"))
 
 NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",

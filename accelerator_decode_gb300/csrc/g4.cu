@@ -31,6 +31,7 @@
 #include <vector>
 
 #include "attn.cuh"
+#include "attn_mqa.cuh"
 #include "common.cuh"
 #include "gemm_tc.cuh"
 #include "gemv.cuh"
@@ -384,6 +385,8 @@ void attrs_staged(int optin) {
 }
 template <int D>
 void attrs_attn(int optin) {
+  set_max_dyn(attn_mqa_kernel<D, false>, optin);
+  set_max_dyn(attn_mqa_kernel<D, true>, optin);
   set_max_dyn(attn_kernel<D, 1, false>, optin);
   set_max_dyn(attn_kernel<D, 1, true>, optin);
   carve_max(kv_write_kernel<D, false>);
@@ -795,7 +798,27 @@ void launch_attn_d(const AttnArgs& a, int hpc, int nb, bool kv8, cudaStream_t st
   if (kv8) launch_attn<D, 1, true>(a, nb, st);
   else launch_attn<D, 1, false>(a, nb, st);
 }
-void launch_attn_any(const AttnArgs& a, int d, int hpc, int nb, bool kv8, cudaStream_t st) {
+template <int D, bool KV8>
+void launch_mqa(const AttnArgs& a, int nb, cudaStream_t st) {
+  launch(attn_mqa_kernel<D, KV8>, dim3(a.nsplit, nb), dim3(kMqaThreads), mqa_smem_bytes<D, KV8>(a.nstage), st, a);
+}
+template <int D>
+void launch_mqa_d(const AttnArgs& a, int nb, bool kv8, cudaStream_t st) {
+  if (kv8) launch_mqa<D, true>(a, nb, st);
+  else launch_mqa<D, false>(a, nb, st);
+}
+// mqa: the kernel that serves every query head of a sequence from one K/V tile load
+// (attn_mqa.cuh); else one CTA per (split, head) (attn.cuh).
+void launch_attn_any(const AttnArgs& a, int d, int hpc, int nb, bool kv8, bool mqa, cudaStream_t st) {
+  if (mqa) {
+    switch (d) {
+      case 64: launch_mqa_d<64>(a, nb, kv8, st); break;
+      case 128: launch_mqa_d<128>(a, nb, kv8, st); break;
+      case 256: launch_mqa_d<256>(a, nb, kv8, st); break;
+      default: launch_mqa_d<512>(a, nb, kv8, st); break;
+    }
+    return;
+  }
   switch (d) {
     case 64: launch_attn_d<64>(a, hpc, nb, kv8, st); break;
     case 128: launch_attn_d<128>(a, hpc, nb, kv8, st); break;
@@ -834,6 +857,34 @@ int attn_nsplit(int sms, int nq, int hpc, int nb, int max_keys) {
   int ns = cdiv(2 * sms, nb * n_hg);
   ns = std::min(ns, std::max(1, cdiv(max_keys, kAttnTile)));
   return std::max(1, std::min(ns, 64));
+}
+// The MQA kernel: one CTA per (split, sequence); about two per SM.
+int mqa_nsplit(int sms, int nb, int max_keys) {
+  int ns = cdiv(2 * sms, nb);
+  ns = std::min(ns, std::max(1, cdiv(max_keys, kAttnTile)));
+  return std::max(1, std::min(ns, 64));
+}
+// From this many sequences on, attention runs the MQA kernel (G4_ATTN_MQA_MIN; 0 disables
+// it).  Below, one CTA per (split, head) keeps a single sequence's latency short: the MQA
+// kernel has fewer CTAs to spread one sequence's keys over and a longer merge.
+int mqa_min_batch() {  // read at every plan (a graph keeps the choice it was captured with)
+  const char* e = getenv("G4_ATTN_MQA_MIN");
+  return e ? atoi(e) : 8;
+}
+bool mqa_on(int nq, int n) { return mqa_min_batch() > 0 && n >= mqa_min_batch() && nq <= kMqaMaxHeads; }
+// Splits and tile buffers of an attention launch over n sequences (either kernel).
+void attn_plan(int sms, int nq, int n, int d, int max_keys, AttnArgs& a) {
+  if (mqa_on(nq, n)) {
+    a.nsplit = mqa_nsplit(sms, n, max_keys);
+    a.nstage = (d <= 256 && cdiv(max_keys, a.nsplit) > kAttnTile) ? 2 : 1;
+    return;
+  }
+  const int hpc = attn_hpc(nq, n);
+  a.nsplit = attn_nsplit(sms, nq, hpc, n, max_keys);
+  // double-buffered K/V tiles only while the grid fits on the SMs at one unit each: a
+  // larger grid needs the occupancy more than the overlap (the 512-wide tiles take 128 KB)
+  const long units = (long)n * (nq / hpc) * a.nsplit;
+  a.nstage = (cdiv(max_keys, a.nsplit) > kAttnTile && units <= sms) ? 2 : 1;
 }
 
 // ------------------------------------------------------------------------------- profiler
@@ -917,14 +968,12 @@ void launch_layer_attn(g4_handle* h, const Layer& Y, const float* qkv, int qkv_s
   a.out_stride = c.num_q_heads * Y.d;
   const int hpc = attn_hpc(c.num_q_heads, n);
   const int max_keys = Y.full ? c.max_context : std::min(c.sliding_window, c.max_context);
-  a.nsplit = attn_nsplit(h->sms, c.num_q_heads, hpc, n, max_keys);
-  const long units = (long)n * (c.num_q_heads / hpc) * a.nsplit;
-  a.nstage = (cdiv(max_keys, a.nsplit) > kAttnTile && units <= h->sms) ? 2 : 1;
+  attn_plan(h->sms, c.num_q_heads, n, Y.d, max_keys, a);
   a.ws_ml = h->attn_ml;
   a.ws_o = h->attn_o;
   a.counters = h->attn_cnt;
   a.err = h->err;
-  launch_attn_any(a, Y.d, hpc, n, h->kv8, st);
+  launch_attn_any(a, Y.d, hpc, n, h->kv8, mqa_on(c.num_q_heads, n), st);
 }
 
 // Decode step of 1-4 rows on the staged projections (gemv_s.cuh).  Every projection but the
@@ -1217,18 +1266,14 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.out_stride = nqd;
       const int hpc = attn_hpc(c.num_q_heads, n);
       const int max_keys = Y.full ? c.max_context : std::min(c.sliding_window, c.max_context);
-      a.nsplit = attn_nsplit(h->sms, c.num_q_heads, hpc, n, max_keys);
-      // double-buffered K/V tiles only while the grid fits on the SMs at one unit each: a
-      // larger grid needs the occupancy more than the overlap (the 512-wide tiles take 128 KB)
-      const long units = (long)n * (c.num_q_heads / hpc) * a.nsplit;
-      a.nstage = (cdiv(max_keys, a.nsplit) > kAttnTile && units <= h->sms) ? 2 : 1;
+      attn_plan(h->sms, c.num_q_heads, n, Y.d, max_keys, a);
       a.ws_ml = h->attn_ml;
       a.ws_o = h->attn_o;
       a.counters = h->attn_cnt;
       a.err = h->err;
       ProfScope ps(prof, Y.full ? "attn.full" : "attn.sliding", 0.0);
       if (kv_first && Y.own) launch_kv_write_any(a, Y.d, n, h->kv8, st);
-      launch_attn_any(a, Y.d, hpc, n, h->kv8, st);
+      launch_attn_any(a, Y.d, hpc, n, h->kv8, mqa_on(c.num_q_heads, n), st);
       if (h->trace)
         for (int i = 0; i < n; ++i)
           cudaMemcpyAsync(h->trace + ((size_t)(l * 2) * c.max_batch + i) * ts, h->attn + (size_t)i * nqd,
@@ -1964,8 +2009,9 @@ g4_status create_impl(g4_handle* h, const g4_config* cfg, const g4_weights* w, c
       const int keys = t ? c.max_context : std::min(c.sliding_window, c.max_context);
       const int ns = attn_nsplit(h->sms, nq, hpc, nb, keys);
       const int ns1 = attn_nsplit(h->sms, nq, 1, 1, keys);  // persistent step: nb=1 plan, 2 rows
-      ml = std::max({ml, (size_t)nb * nq * ns * 2, (size_t)2 * nq * ns1 * 2});
-      ao = std::max({ao, (size_t)nb * nq * ns * d, (size_t)2 * nq * ns1 * d});
+      const int nsm = mqa_nsplit(h->sms, nb, keys);
+      ml = std::max({ml, (size_t)nb * nq * ns * 2, (size_t)2 * nq * ns1 * 2, (size_t)nb * nq * nsm * 2});
+      ao = std::max({ao, (size_t)nb * nq * ns * d, (size_t)2 * nq * ns1 * d, (size_t)nb * nq * nsm * d});
     }
   }
   h->attn_ml_n = ml;

@@ -33,6 +33,7 @@ def main(argv=None):
     ap.add_argument("--position", type=int, default=128)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--phases", action="store_true", help="also time every phase (direct launches)")
     a = ap.parse_args(argv)
     cfg = synth.get_config(a.config)
     w = synth.make_model_weights(cfg, a.fmt, seed=a.seed, tables=a.tables)
@@ -52,6 +53,11 @@ def main(argv=None):
             e1.record(st)
             e1.synchronize()
             print(f"step {i}: {e0.elapsed_time(e1) * 1e3:.1f} us", flush=True)
+        if a.phases:
+            prof = dec.profile_step(slots, tok, pos, out, None, repeats=2, stream=st)
+            for ph in prof:
+                print(f"phase {ph['name']:24s} launches {ph['launches'] // 2:4d}  {ph['ms_total'] / 2 * 1e3:9.1f} us/step",
+                      flush=True)
         status, word = dec.device_error(stream=st)
     dec.close()
     if word:

@@ -233,3 +233,20 @@ def test_all_variants_together_e2b_heads(rt):
     assert dec.device_error()[1] == 0
     dec.close()
     check(ref, toks, logits, "int4 tables + int8 paged")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_mqa_attention_kernel_matches_oracle(rt, kv, monkeypatch):
+    """The attention kernel that serves every query head of a sequence from one K/V tile
+    load (used from 8 sequences on), forced on at batch 2: E2B head dims, 300-token prompts,
+    several splits and tiles, the merge."""
+    monkeypatch.setenv("G4_ATTN_MQA_MIN", "1")
+    cfg = synth.get_config("mid")
+    w = synth.make_weights(cfg, "w4a16", seed=27, gain_std=0.1)
+    prompts = synth.make_prompts(cfg["vocab"], 2, 300, seed=41)
+    ref = oracle.Oracle(cfg, w, max_batch=2, max_context=384, kv_dtype=kv).generate(prompts, 8, keep_logits=True)
+    dec = rt.Decoder(cfg, w, max_batch=2, max_context=384, kv_format=kv)
+    toks, logits = forced(dec, list(prompts), ref)
+    assert dec.device_error()[1] == 0
+    dec.close()
+    check(ref, toks, logits, f"mqa {kv}")
