@@ -42,4 +42,13 @@ def test_graph_replay_equals_direct_launches_and_oracle(rt, mode):
     graph.close()
     np.testing.assert_array_equal(t0, t1)
     np.testing.assert_array_equal(l0, l1)
-    check_parity(ref, t1, l1, f"graph replay/mode {mode}")
+    def rerun(teacher):
+        d = rt.Decoder(cfg, w, max_batch=2, max_context=48)
+        d.set_step_mode(mode)
+        with torch.cuda.stream(st):
+            r = gpu_generate(d, list(prompts), 10, teacher=teacher)
+        torch.cuda.synchronize()
+        d.close()
+        return r
+
+    check_parity(ref, t1, l1, f"graph replay/mode {mode}", rerun=rerun)
