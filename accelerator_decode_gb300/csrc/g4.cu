@@ -117,6 +117,10 @@ struct g4_handle {
   int device = 0, sms = 0;
   std::vector<void*> allocs;
   size_t bytes = 0;
+  // allocation-failure injection (tests): the fail_at-th device allocation of g4_create
+  // reports out-of-memory without allocating (G4_FAIL_ALLOC_AT; 0 = off)
+  int fail_at = 0, n_allocs = 0;
+  int* probe_flag = nullptr;  // a flag nothing sets (g4_timeout_probe)
   std::vector<Layer> layers;
   Lin pmp, lm;
   const __nv_bfloat16 *embed = nullptr, *ple_table = nullptr, *g_ppn = nullptr, *g_final = nullptr;
@@ -192,6 +196,7 @@ template <class T>
 g4_status dalloc(g4_handle* h, T** p, size_t count) {
   void* q = nullptr;
   const size_t nbytes = std::max<size_t>(count, 1) * sizeof(T);
+  if (h->fail_at > 0 && ++h->n_allocs == h->fail_at) return G4_ERR_OOM;  // injected
   cudaError_t e = cudaMalloc(&q, nbytes);
   if (e != cudaSuccess) {
     cuda_ok(e, "cudaMalloc");
@@ -2070,6 +2075,7 @@ g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
   g4_handle* h = new g4_handle();
   h->cfg = *cfg;
   h->device = device;
+  if (const char* fa = getenv("G4_FAIL_ALLOC_AT")) h->fail_at = atoi(fa);
   cudaError_t e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device);
   if (!cuda_ok(e, "cudaDeviceGetAttribute")) { delete h; return G4_ERR_CUDA; }
   cudaStream_t st = nullptr;
@@ -2079,6 +2085,7 @@ g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
   cudaStreamSynchronize(st);
   cudaStreamDestroy(st);
   if (s != G4_OK) { destroy(h); return s; }
+  h->fail_at = 0;  // the hook covers g4_create only
   *out = h;
   return G4_OK;
 }
@@ -2369,6 +2376,19 @@ g4_status g4_profile_step(g4_handle* h, g4_stream stream, int32_t n_seq, const i
     stats[k++] = agg[nm];
   }
   *n_stats = k;
+  return G4_OK;
+}
+
+g4_status g4_timeout_probe(g4_handle* h, g4_stream stream, int64_t wait_ns) {
+  if (!h || wait_ns < 0 || wait_ns > 2000000000LL) return G4_ERR_INVALID_ARG;
+  DEVICE_GUARD(h->device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!h->probe_flag) {
+    TRY(dalloc(h, &h->probe_flag, 1));
+    CK(cudaMemsetAsync(h->probe_flag, 0, sizeof(int), st));
+  }
+  probe_wait_kernel<<<1, 32, 0, st>>>(h->probe_flag, (unsigned long long)wait_ns, h->err);
+  CK(cudaGetLastError());
   return G4_OK;
 }
 

@@ -243,4 +243,20 @@ __global__ void argmax_rows_kernel(const float* logits, int n_cols, int chunk, f
   }
 }
 
+// Failure-detection probe: one warp waits for *flag to become non-zero, checking
+// %globaltimer, and gives up after wait_ns: the timeout bit goes to the error word and the
+// kernel returns (the wait always ends; the context stays usable).  Nothing sets the flag
+// the library passes, so the probe exercises the bounded-wait path of the step's kernels.
+__global__ void probe_wait_kernel(const int* flag, unsigned long long wait_ns, int* err) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    if (*reinterpret_cast<const volatile int*>(flag) != 0) return;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > wait_ns) break;
+    __nanosleep(1000);
+  }
+  if (threadIdx.x == 0) set_err(err, G4_DEV_TIMEOUT);
+}
+
 }  // namespace g4

@@ -96,6 +96,7 @@ def _load():
                                     POINTER(c_int32)]),
         "g4_free": (None, [P]),
         "g4_kv_reserve": (c_int, [P, P, c_int32, c_int32]),
+        "g4_timeout_probe": (c_int, [P, P, c_int64]),
         "g4_kv_release": (c_int, [P, P, c_int32]),
         "g4_kv_pages_free": (c_int32, [P]),
         "g4_status_string": (ctypes.c_char_p, [c_int]),

@@ -136,6 +136,9 @@ typedef struct g4_handle g4_handle;
  * Errors: G4_ERR_INVALID_ARG, G4_ERR_UNSUPPORTED, G4_ERR_OOM, G4_ERR_CUDA (nothing leaks). */
 g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
                     g4_handle** out);
+/* Testing hook: with the environment variable G4_FAIL_ALLOC_AT=n (n >= 1), the n-th device
+ * allocation of a g4_create call reports out-of-memory without allocating; g4_create then
+ * frees everything it took and returns G4_ERR_OOM. */
 
 /* Prefill (teacher-forced): for each sequence i, feed tokens d_tokens[offsets[i] ..
  * offsets[i+1]) at positions start_pos[i] + 0, 1, ... of cache slot slots[i], writing the
@@ -181,6 +184,13 @@ g4_status g4_kv_release(g4_handle* h, g4_stream stream, int32_t slot);
 
 /* Free pool pages (paged KV cache), or -1 with static rows or a NULL handle. */
 int32_t g4_kv_pages_free(const g4_handle* h);
+
+/* Failure-detection probe (tests): launch one warp on `stream` that waits, bounded by
+ * wait_ns of %globaltimer, for a device flag that nothing sets; when the wait runs out it sets
+ * G4_DEV_TIMEOUT in the device error word and returns, as every bounded wait of the step's
+ * kernels does.  The next g4_get_device_error then returns G4_ERR_TIMEOUT and the handle stays
+ * usable.  Errors: G4_ERR_INVALID_ARG (wait_ns outside 0..2e9). */
+g4_status g4_timeout_probe(g4_handle* h, g4_stream stream, int64_t wait_ns);
 
 /* Synchronise `stream`, read and clear the device error word.  *word_out (nullable) gets
  * the G4_DEV_* bits.  Returns G4_ERR_TIMEOUT if the timeout bit is set, else
