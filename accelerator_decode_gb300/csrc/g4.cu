@@ -691,7 +691,7 @@ void run_gemm(const Lin& L, int epi, const GemvIO& io, int n, float eps, const T
   p.kpad = nkb * kTcKB;
   p.bpad = bpad;
   p.xt = s.xt;
-  launch(prep_x_kernel, dim3(n), dim3(256), prep_smem_bytes(p.kpad), st, p);
+  launch(prep_x_kernel, dim3(n), dim3(256), prep_smem_bytes(p.kpad, p.pro), st, p);
   GemmArgs g{};
   g.qw = L.qw;
   g.sc = L.sc;

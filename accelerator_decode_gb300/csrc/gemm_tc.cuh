@@ -54,6 +54,11 @@ struct GemmArgs {
 __host__ __device__ inline size_t tc_stage_bytes(int bpad) {
   return 16384 /* raw weights (+scales) */ + 16384 /* A tile */ + (size_t)2 * bpad * 128 /* x parts */;
 }
+// The split-K merge (a 4-deep ring of [bpad/4][128] float4 partials) and the epilogue's two
+// [bpad][128] float buffers reuse the stage buffers once the accumulator is complete: they
+// must fit in them for every bpad up to 64.
+static_assert(4 * 128 * 64 * 4 + 2 * 64 * 128 * 4 <= kTcStages * (16384 + 16384 + 2 * 64 * 128),
+              "merge and epilogue buffers exceed the stage buffers");
 __host__ __device__ inline size_t tc_smem_bytes(int bpad) {
   return 1024 /* alignment slack */ + kTcStages * tc_stage_bytes(bpad) + 256 /* barriers, flags */;
 }
@@ -137,8 +142,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
   const int nkb = kb1 - kb0;
   const int ncols = a.bpad <= 32 ? 32 : (a.bpad <= 64 ? 64 : 128);
 
-  pdl_wait();
-  pdl_trigger();
+  // barriers, TMEM and the first stages' weights do not depend on the previous kernel: they
+  // are set up and requested before the dependency wait (only the producer's activation
+  // copies and the other warps' work come after it)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTcStages; ++s) {
       mbar_init(&full[s], 1);
@@ -167,17 +173,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     // ---------------- TMA producer
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % kTcStages, r = i / kTcStages;
-        if (r > 0 && !mbar_wait(&mdone[s], (r - 1) & 1, abort_flag)) {
-          set_err(a.err, G4_DEV_TIMEOUT);
-          *abort_flag = 1;
-          break;
-        }
+      const uint32_t wbytes = w4 ? 4 * 1024 : 4 * 4096;
+      const uint32_t sbytes = w4 ? 4 * 512 : 0;
+      auto weights = [&](int i) {  // stage i's weight (and scale) copies
+        const int s = i % kTcStages;
         uint8_t* st = stage0 + s * stage_bytes;
         const int kb = kb0 + i;
-        const uint32_t wbytes = w4 ? 4 * 1024 : 4 * 4096;
-        const uint32_t sbytes = w4 ? 4 * 512 : 0;
         mbar_expect_tx(&full[s], wbytes + sbytes + 2 * xbytes);
         for (int rb = 0; rb < 4; ++rb) {
           const size_t grb = (size_t)mt * 4 + rb;
@@ -191,8 +192,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
             bulk_g2s(st + rb * 4096, src, 4096, &full[s]);
           }
         }
-        const uint8_t* xsrc = a.xt + (size_t)kb * 2 * xbytes;
-        bulk_g2s(st + 32768, xsrc, 2 * xbytes, &full[s]);
+      };
+      auto acts = [&](int i) {  // stage i's activation tiles (written by the previous kernel)
+        const int s = i % kTcStages;
+        const uint8_t* xsrc = a.xt + (size_t)(kb0 + i) * 2 * xbytes;
+        bulk_g2s(stage0 + s * stage_bytes + 32768, xsrc, 2 * xbytes, &full[s]);
+      };
+      const int npre = min(nkb, kTcStages);
+      for (int i = 0; i < npre; ++i) weights(i);
+      pdl_wait();
+      pdl_trigger();
+      for (int i = 0; i < npre; ++i) acts(i);
+      issued = npre;
+      for (int i = npre; i < nkb; ++i) {
+        const int s = i % kTcStages, r = i / kTcStages;
+        if (r > 0 && !mbar_wait(&mdone[s], (r - 1) & 1, abort_flag)) {
+          set_err(a.err, G4_DEV_TIMEOUT);
+          *abort_flag = 1;
+          break;
+        }
+        weights(i);
+        acts(i);
         ++issued;
       }
       if (*abort_flag) {
@@ -202,6 +222,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer
+    pdl_wait();
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(a.bpad);
       bool ok = true;
@@ -240,6 +261,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     }
   } else {
     // ---------------- dequant warps: thread m owns weight row m of the M tile
+    pdl_wait();
     const int m = threadIdx.x;  // 0..127
     const int rbl = m >> 5, ln = m & 31;
     for (int i = 0; i < nkb; ++i) {
@@ -449,7 +471,9 @@ struct PrepArgs {
 
 // Shared memory of prep_x_kernel: x row and residual branch (fp32, kpad each), then both gain
 // vectors (bf16, kpad each).
-__host__ __device__ inline size_t prep_smem_bytes(int kpad) { return (size_t)kpad * (2 * 4 + 2 * 2); }
+__host__ __device__ inline size_t prep_smem_bytes(int kpad, int pro) {
+  return pro == PRO_PLAIN ? (size_t)kpad * 4 : (size_t)kpad * (2 * 4 + 2 * 2);  // plain: the x row only
+}
 
 __global__ void __launch_bounds__(256) prep_x_kernel(const PrepArgs a) {
   extern __shared__ __align__(16) float prow[];  // [kpad] | residual [kpad] | g_r, g_a [kpad] bf16
