@@ -115,7 +115,7 @@ def algorithmic_bytes(cfg, fmt, batch, positions, count_aliased=False, tables="b
 # DRAM traffic / algorithmic bytes of a kernel, from one ncu capture of its current code;
 # traffic scales with the rows a launch streams.
 # Keyed by (weight format, phase); a kernel changed since its capture has no entry.
-MEASURED_TRAFFIC_RATIO = {}
+MEASURED_TRAFFIC_RATIO = {("w4a16", "gemv.gate_up"): 10717952 / 10616832}
 
 
 def measured_peak():
@@ -231,7 +231,7 @@ def run_gpu(args, wl, cfg, fmt):
     weights = synth.make_model_weights(cfg, fmt, seed=args.seed)
     prompts = synth.make_prompts(cfg["vocab"], B, P0, seed=args.seed, stream=rank)
     t_gen = time.perf_counter() - t_gen
-    dec = Decoder(cfg, weights, max_batch=B, max_context=max_ctx, device=local)
+    dec = Decoder(cfg, weights, max_batch=B, max_context=max_ctx, device=local, kv_format=args.kv)
     if args.step_mode:
         dec.set_step_mode(args.step_mode)
     step_mode = dec.step_mode(B)
@@ -333,8 +333,8 @@ def run_gpu(args, wl, cfg, fmt):
 
 
     positions = [P0 + i for i in range(K)]
-    wbytes, kvbytes = algorithmic_bytes(cfg, fmt, B, positions)
-    _, kv_aliased = algorithmic_bytes(cfg, fmt, B, positions, count_aliased=True)
+    wbytes, kvbytes = algorithmic_bytes(cfg, fmt, B, positions, kv=args.kv)
+    _, kv_aliased = algorithmic_bytes(cfg, fmt, B, positions, count_aliased=True, kv=args.kv)
     peak, peak_src = measured_peak()
     step_bytes = wbytes + kvbytes
     value = replica_throughput(world, B, K, ms_max)
@@ -370,8 +370,8 @@ def run_gpu(args, wl, cfg, fmt):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl["name"], "weights": fmt, "batch_per_gpu": B, "prompt_tokens": P0,
-                   "decode_positions": [P0, P0 + K - 1], "parallelism": f"replicas x{world}",
+        "config": {"workload": wl["name"], "weights": fmt, "kv_cache": args.kv, "batch_per_gpu": B,
+                   "prompt_tokens": P0, "decode_positions": [P0, P0 + K - 1], "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (weights streamed every step exceed 129 MB)",
                    "seed": args.seed,
                    "knobs": {k: os.environ[k] for k in ("G4_TC_MIN_BATCH", "G4_GEMV_UNSPLIT_BYTES")
@@ -491,7 +491,7 @@ def run_replay(args, wl, cfg, fmt):
     max_ctx = sched[0][0] + sum(a + o for a, o in sched[1:])
     max_ctx = ((max_ctx + 63) // 64) * 64
     weights = synth.make_model_weights(cfg, fmt, seed=args.seed)
-    dec = Decoder(cfg, weights, max_batch=B, max_context=max_ctx, device=local)
+    dec = Decoder(cfg, weights, max_batch=B, max_context=max_ctx, device=local, kv_format=args.kv)
     dev = torch.device("cuda", local)
     st = torch.cuda.Stream()
     slots = list(range(B))
@@ -550,7 +550,8 @@ def run_replay(args, wl, cfg, fmt):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": wl["name"], "weights": fmt, "batch_per_gpu": B, "start_context": sched[0][0],
+        "config": {"workload": wl["name"], "weights": fmt, "kv_cache": args.kv, "batch_per_gpu": B,
+                   "start_context": sched[0][0],
                    "final_context": ctx[0], "turns": turns, "outputs_per_turn": n_out},
         "by_context": rows,
         "clocks": clk,
@@ -611,6 +612,7 @@ def main(argv=None):
                     help="skip the companion figures (batch 64, bf16, int4 tables + int8 cache)")
     ap.add_argument("--no-companions", dest="companions", action="store_false",
                     help="keep the batch-64 figure, skip the bf16 and int4-table / int8-cache ones")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"], help="KV cache rows (default bf16)")
     ap.add_argument("--impl-check-only", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -25,6 +25,8 @@
  *     with g4_get_device_error.
  *   - All functions are thread-compatible, not thread-safe: one handle, one host thread at
  *     a time.
+ *   - Entry points that take a handle or a device index make that device current for the
+ *     call and restore the caller's current device before returning.
  */
 #ifndef G4_H
 #define G4_H
@@ -142,7 +144,12 @@ g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
 
 /* Prefill (teacher-forced): for each sequence i, feed tokens d_tokens[offsets[i] ..
  * offsets[i+1]) at positions start_pos[i] + 0, 1, ... of cache slot slots[i], writing the
- * K/V of every position ("jitted prefill").  Appending to an existing context is start_pos >
+ * K/V of every position ("Gemma 4 E2B in JAX on One TPU v5e", Step 2: jitted prefill into a
+ * static cache).  The problem statement passes slots, offsets and start positions as device
+ * arrays; here they are HOST arrays (a reading): the prompt rows are planned into blocks of up
+ * to 64 and, with a paged cache, pages are reserved on the host before any launch, both from
+ * the lengths, so device metadata would cost a device-to-host copy and a synchronisation per
+ * call.  The token ids stay on the device.  Appending to an existing context is start_pos >
  * 0.  d_next_ids[i] = greedy argmax after the sequence's last token; d_logits (nullable)
  * receives those logits [n_seq, vocab] fp32.  slots, offsets, start_pos are HOST arrays
  * (n_seq, n_seq + 1, n_seq entries); d_tokens is a DEVICE array of offsets[n_seq] ids.
