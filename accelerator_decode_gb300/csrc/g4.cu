@@ -718,7 +718,8 @@ void run_gemm(const Lin& L, int epi, const GemvIO& io, int n, float eps, const T
   g.n_mtiles = L.n_rb / 4;
   g.err = s.err;
   const int grid = g.n_mtiles * g.ksplit;
-  launch(gemm_tc_kernel, dim3(grid), dim3(kTcThreads), tc_smem_bytes(bpad), st, g);
+  g.stages = g.ksplit > 1 ? kTcStages : 2;
+  launch(gemm_tc_kernel, dim3(grid), dim3(kTcThreads), tc_smem_bytes(bpad, g.stages), st, g);
   if (epi == EPI_ARGMAX)
     launch(argmax_partials_kernel, dim3(n), dim3(256), 0, st, (const float*)s.am_val, (const int*)s.am_idx, grid,
            io.next_ids);

@@ -21,7 +21,7 @@
 
 namespace g4 {
 
-constexpr int kTcStages = 4;
+constexpr int kTcStages = 4;      // ring stages with a K split (the merge reuses them); 2 without
 constexpr int kTcThreads = 192;        // warps 0-3 dequant/epilogue, 4 TMA + TMEM alloc, 5 MMA
 constexpr int kTcM = 128;
 constexpr int kTcKB = 64;              // k per block
@@ -46,6 +46,7 @@ struct GemmArgs {
   float* am_val;         // [nb][gridDim.x]
   int* am_idx;
   float* part;           // [ksplit][n_mtiles * 128 rows][64 columns]
+  int stages;            // ring stages: kTcStages, or 2 when ksplit == 1 (two CTAs per SM)
   unsigned* counters;    // per M tile
   int n_mtiles;
   int* err;
@@ -55,12 +56,14 @@ __host__ __device__ inline size_t tc_stage_bytes(int bpad) {
   return 16384 /* raw weights (+scales) */ + 16384 /* A tile */ + (size_t)2 * bpad * 128 /* x parts */;
 }
 // The split-K merge (a 4-deep ring of [bpad/4][128] float4 partials) and the epilogue's two
-// [bpad][128] float buffers reuse the stage buffers once the accumulator is complete: they
-// must fit in them for every bpad up to 64.
+// [bpad][128] float buffers reuse the stage buffers once the accumulator is complete: with a
+// K split the ring and the buffers must fit in kTcStages stages, without one (2 stages, no
+// ring) the buffers alone in 2, for every bpad up to 64.
 static_assert(4 * 128 * 64 * 4 + 2 * 64 * 128 * 4 <= kTcStages * (16384 + 16384 + 2 * 64 * 128),
               "merge and epilogue buffers exceed the stage buffers");
-__host__ __device__ inline size_t tc_smem_bytes(int bpad) {
-  return 1024 /* alignment slack */ + kTcStages * tc_stage_bytes(bpad) + 256 /* barriers, flags */;
+static_assert(2 * 64 * 128 * 4 <= 2 * (16384 + 16384 + 2 * 16 * 128), "epilogue buffers exceed two stages");
+__host__ __device__ inline size_t tc_smem_bytes(int bpad, int stages) {
+  return 1024 /* alignment slack */ + stages * tc_stage_bytes(bpad) + 256 /* barriers, flags */;
 }
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -126,7 +129,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_raw_smem) + 1023) & ~uintptr_t(1023));
   const size_t stage_bytes = tc_stage_bytes(a.bpad);
   uint8_t* stage0 = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kTcStages * stage_bytes);
+  const int NS = a.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * stage_bytes);
   uint64_t* full = bars;                     // [kTcStages] TMA data landed
   uint64_t* aready = bars + kTcStages;       // [kTcStages] dequantised tile written
   uint64_t* mdone = bars + 2 * kTcStages;    // [kTcStages] MMAs of the stage finished
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
   // are set up and requested before the dependency wait (only the producer's activation
   // copies and the other warps' work come after it)
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&aready[s], 128);
       mbar_init(&mdone[s], 1);
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
       const uint32_t wbytes = w4 ? 4 * 1024 : 4 * 4096;
       const uint32_t sbytes = w4 ? 4 * 512 : 0;
       auto weights = [&](int i) {  // stage i's weight (and scale) copies
-        const int s = i % kTcStages;
+        const int s = i % NS;
         uint8_t* st = stage0 + s * stage_bytes;
         const int kb = kb0 + i;
         mbar_expect_tx(&full[s], wbytes + sbytes + 2 * xbytes);
@@ -194,18 +198,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
         }
       };
       auto acts = [&](int i) {  // stage i's activation tiles (written by the previous kernel)
-        const int s = i % kTcStages;
+        const int s = i % NS;
         const uint8_t* xsrc = a.xt + (size_t)(kb0 + i) * 2 * xbytes;
         bulk_g2s(stage0 + s * stage_bytes + 32768, xsrc, 2 * xbytes, &full[s]);
       };
-      const int npre = min(nkb, kTcStages);
+      const int npre = min(nkb, NS);
       for (int i = 0; i < npre; ++i) weights(i);
       pdl_wait();
       pdl_trigger();
       for (int i = 0; i < npre; ++i) acts(i);
       issued = npre;
       for (int i = npre; i < nkb; ++i) {
-        const int s = i % kTcStages, r = i / kTcStages;
+        const int s = i % NS, r = i / NS;
         if (r > 0 && !mbar_wait(&mdone[s], (r - 1) & 1, abort_flag)) {
           set_err(a.err, G4_DEV_TIMEOUT);
           *abort_flag = 1;
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
       }
       if (*abort_flag) {
         // drain: every issued stage must land before the CTA exits
-        for (int i = 0; i < issued; ++i) mbar_wait_drain(&full[i % kTcStages], (i / kTcStages) & 1);
+        for (int i = 0; i < issued; ++i) mbar_wait_drain(&full[i % NS], (i / NS) & 1);
       }
     }
   } else if (warp == 5) {
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
       const uint32_t idesc = umma_idesc_bf16(a.bpad);
       bool ok = true;
       for (int i = 0; i < nkb; ++i) {
-        const int s = i % kTcStages, r = i / kTcStages;
+        const int s = i % NS, r = i / NS;
         if (!mbar_wait(&aready[s], r & 1, abort_flag)) { ok = false; break; }
         asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
         uint8_t* st = stage0 + s * stage_bytes;
@@ -265,7 +269,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     const int m = threadIdx.x;  // 0..127
     const int rbl = m >> 5, ln = m & 31;
     for (int i = 0; i < nkb; ++i) {
-      const int s = i % kTcStages, r = i / kTcStages;
+      const int s = i % NS, r = i / NS;
       if (!mbar_wait(&full[s], r & 1, abort_flag)) {
         set_err(a.err, G4_DEV_TIMEOUT);
         *abort_flag = 1;
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const GemmArgs a
     // ring, which other threads may still be reading), and the variants below run as rolled
     // loops over b: fully unrolled 64-column epilogues ran once per CTA from a cold
     // instruction cache.  The stage buffers are idle once the accumulator is complete.
-    float* ex = reinterpret_cast<float*>(stage0 + (size_t)4 * kTcM * a.bpad * 4);  // [bpad][128]
+    float* ex = reinterpret_cast<float*>(stage0 + (a.ksplit > 1 ? (size_t)4 * kTcM * a.bpad * 4 : 0));  // [bpad][128]
     float* pl = ex + (size_t)a.bpad * kTcM;                                        // [bpad][128]
     if (final_ok) {
 #pragma unroll
