@@ -119,22 +119,17 @@ def test_int8_kv_long_context_e2b_heads(rt):
     check(ref, toks, logits, "int8 mid 600")
 
 
-@pytest.mark.parametrize("kv", ["bf16", "int8"])
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("kv,mode", [("bf16", 0), ("bf16", 1), ("int8", 0)])
 def test_paged_matches_oracle_out_of_order_pages(rt, kv, mode):
     """Pages of 16 positions, handed out interleaved between two sequences (neither holds a
-    contiguous run of pool pages); mode 1 runs the persistent step where it is available."""
+    contiguous run of pool pages); mode 1 runs the persistent step (bf16 rows only)."""
     cfg = synth.get_config("tiny10")
     w = synth.make_weights(cfg, "w4a16", seed=9, gain_std=0.1)
     prompts = synth.make_prompts(cfg["vocab"], 2, 30, seed=12)
     ref = oracle.Oracle(cfg, w, max_batch=2, max_context=96, kv_dtype=kv).generate(prompts, 20, keep_logits=True)
     dec = rt.Decoder(cfg, w, max_batch=2, max_context=96, kv_format=kv, kv_page_size=16)
     if mode == 1:
-        try:
-            dec.set_step_mode(1)
-        except Exception:
-            dec.close()
-            pytest.skip("no persistent step for this cache format")
+        dec.set_step_mode(1)
     total = dec.pages_free()
     assert total == 2 * 6
     for n in range(16, 64, 16):             # interleave: slot 0 and slot 1 alternate pages
@@ -250,3 +245,23 @@ def test_mqa_attention_kernel_matches_oracle(rt, kv, monkeypatch):
     assert dec.device_error()[1] == 0
     dec.close()
     check(ref, toks, logits, f"mqa {kv}")
+
+
+def test_persistent_step_refuses_int8_rows_and_int4_tables(rt):
+    """The persistent step reads bf16 cache rows and tables only: asking for it with int8 rows
+    or int4 tables is refused on the host, and the default path keeps working."""
+    from accelerator_decode_gb300 import g4
+    cfg = synth.get_config("tiny")
+    for kw, tables in (({"kv_format": "int8"}, "bf16"), ({}, "int4")):
+        w = synth.make_weights(cfg, "bf16", seed=2, tables=tables)
+        dec = rt.Decoder(cfg, w, max_batch=1, max_context=32, **kw)
+        with pytest.raises(g4.G4Error) as e:
+            dec.set_step_mode(1)
+        assert e.value.status == g4.G4_ERR_UNSUPPORTED
+        assert dec.step_mode(1) == 0
+        prompts = synth.make_prompts(cfg["vocab"], 1, 8, seed=2)
+        ref = oracle.Oracle(cfg, w, max_batch=1, max_context=32,
+                            kv_dtype=kw.get("kv_format", "bf16")).generate(prompts, 4, keep_logits=True)
+        toks, logits = forced(dec, list(prompts), ref)
+        dec.close()
+        check(ref, toks, logits, f"refused persistent step {kw} {tables}")
