@@ -36,6 +36,8 @@ struct AttnArgs {
   float scale;
   int window;              // 0 = full attention
   int own;                 // write K/V of this position
+  int early;               // request the first K/V tiles before the dependency wait (no kernel
+                           // right before this one writes cache rows: not behind kv_write_kernel)
   void* kc;                // cache of the source layer: rows of D bf16 or D int8 (KV8)
   void* vc;
   float* ksc;              // KV8: fp32 scale per row
@@ -168,8 +170,10 @@ __device__ __forceinline__ void kv_row(const AttnArgs& a, const float* qraw, int
 // attn_smem_bytes<D, HPC>(a.nstage) bytes.  Called by attn_kernel and by the persistent step.
 template <int D, int HPC, bool KV8 = false>
 // Threads [tid_base, tid_base + 128) run the unit and synchronise on named barrier bar_id.
+// dep_wait: the unit is a kernel of its own behind a programmatic dependency; it requests its
+// first K/V tiles, then waits for the previous kernel (see below).
 __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, int b, unsigned char* asmem,
-                                          int tid_base, int bar_id) {
+                                          int tid_base, int bar_id, bool dep_wait = false) {
   constexpr int PL = D / 32;                                    // q/k elements per lane (scores)
   constexpr int PT = D >= kAttnThreads ? D / kAttnThreads : 1;  // output elements per thread
   static_assert(PL >= 2 && PL % 2 == 0, "head dim must be a multiple of 64");
@@ -210,6 +214,10 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   const unsigned char* kbase = reinterpret_cast<const unsigned char*>(a.kc);
   const unsigned char* vbase = reinterpret_cast<const unsigned char*>(a.vc);
   const int slot0 = slot < 0 ? 0 : slot;
+  if (dep_wait && !a.early) {  // the previous kernel wrote cache rows this unit reads
+    pdl_wait();
+    pdl_trigger();
+  }
 
   // tile loader: keys [t0, t0 + 32) clipped to j1; rows past it (or without a page) are
   // zero-filled, with zero scales
@@ -241,6 +249,16 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
   };
   if (ntiles > 0) load_tile(0);
   if (ntiles > 1 && a.nstage > 1) load_tile(1);
+  // In a decode step the cache rows a unit reads were final before this kernel launched
+  // (earlier steps, or the source layer's launch earlier in this step), except the new row of
+  // an owning layer, which this kernel writes and substitutes from registers (use_new);
+  // positions, slots and page tables are the step's inputs.  So there the first tiles are
+  // requested before waiting for the previous kernel; q (its output) and every write come
+  // after.
+  if (dep_wait && a.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   // ---- q: per-head RMSNorm then RoPE at position p, in registers.  Every global value is
   // loaded before the first shared-memory store: a load issued after a store through another
@@ -544,9 +562,7 @@ __device__ __forceinline__ void attn_unit(const AttnArgs& a, int split, int hg, 
 template <int D, int HPC, bool KV8>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   extern __shared__ __align__(16) unsigned char asmem_k[];
-  pdl_wait();
-  pdl_trigger();
-  attn_unit<D, HPC, KV8>(a, blockIdx.x, blockIdx.y, blockIdx.z, asmem_k, 0, 1);
+  attn_unit<D, HPC, KV8>(a, blockIdx.x, blockIdx.y, blockIdx.z, asmem_k, 0, 1, true);
 }
 
 // K/V rows of an owning layer for every row of a step before its attention runs (prefill

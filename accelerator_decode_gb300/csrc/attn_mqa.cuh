@@ -65,8 +65,6 @@ __global__ void __launch_bounds__(kMqaThreads) attn_mqa_kernel(const AttnArgs a)
   int* is_last_p = reinterpret_cast<int*>(wgt + 64);
   float* kvs_new = wgt + 68;                            // KV8: scales of the new K and V rows
 
-  pdl_wait();
-  pdl_trigger();
   const int split = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nq = a.nq;
@@ -87,6 +85,10 @@ __global__ void __launch_bounds__(kMqaThreads) attn_mqa_kernel(const AttnArgs a)
   const unsigned char* kbase = reinterpret_cast<const unsigned char*>(a.kc);
   const unsigned char* vbase = reinterpret_cast<const unsigned char*>(a.vc);
   const int slot0 = slot < 0 ? 0 : slot;
+  if (!a.early) {  // the previous kernel wrote cache rows this launch reads
+    pdl_wait();
+    pdl_trigger();
+  }
 
   // tile loader: keys [t0, t0 + 32) clipped to j1; rows past it (or without a page) are
   // zero-filled, with zero scales
@@ -118,6 +120,13 @@ __global__ void __launch_bounds__(kMqaThreads) attn_mqa_kernel(const AttnArgs a)
   };
   if (ntiles > 0) load_tile(0);
   if (ntiles > 1 && a.nstage > 1) load_tile(1);
+  // in a decode step, cache rows, positions, slots and page tables were final before this
+  // launch (the new row of an owning layer is patched in from registers): the first tiles go
+  // out before waiting for the previous kernel, whose output (q) is read after it
+  if (a.early) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   // ---- q of every head (warp per head): RMSNorm, gain, RoPE at p; then the new K/V row
   const float* qraw = a.qkv + (size_t)b * a.qkv_stride;

@@ -963,6 +963,7 @@ void launch_layer_attn(g4_handle* h, const Layer& Y, const float* qkv, int qkv_s
   a.scale = Y.scale;
   a.window = Y.full ? 0 : c.sliding_window;
   a.own = own;
+  a.early = 1;  // decode: no kernel right before writes cache rows
   kv_args(h, Src, a);
   a.t_max = c.max_context;
   a.max_batch = c.max_batch;
@@ -1261,6 +1262,7 @@ g4_status run_step(g4_handle* h, cudaStream_t st, int n, const int* d_slots, con
       a.scale = Y.scale;
       a.window = Y.full ? 0 : c.sliding_window;
       a.own = Y.own && !kv_first;
+      a.early = kv_first ? 0 : 1;  // prefill blocks: kv_write_kernel just wrote the rows
       kv_args(h, Src, a);
       a.t_max = c.max_context;
       a.max_batch = c.max_batch;
