@@ -188,6 +188,7 @@ struct g4_handle {
   int* mega_am_idx = nullptr;
   // graphs
   std::map<GraphKey, cudaGraphExec_t> graphs;
+  int smem_optin = 48 * 1024;  // opt-in dynamic shared memory per CTA on this device
 };
 
 namespace {
@@ -387,6 +388,9 @@ void attrs_staged(int optin) {
   set_max_dyn(gemv_s_kernel<FMT, 1, 1, EPI_STORE>, optin);
   set_max_dyn(gemv_s_kernel<FMT, 1, 2, EPI_STORE>, optin);
   set_max_dyn(gemv_s_kernel<FMT, 1, 4, EPI_STORE>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, 1, 1, EPI_ARGMAX>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, 1, 2, EPI_ARGMAX>, optin);
+  set_max_dyn(gemv_s_kernel<FMT, 1, 4, EPI_ARGMAX>, optin);
 }
 template <int D>
 void attrs_attn(int optin) {
@@ -504,6 +508,7 @@ SPlan plan_staged(const Lin& L, int NB, int pro, int norm_n, bool whole_sums, in
       p.a.C = C;
       p.a.spc = spc;
       p.a.cap = cap;
+      p.a.ru = cap;
       p.grid = per * C;
     }
   }
@@ -640,6 +645,105 @@ bool run_staged(const Lin& L, const StagedIn& in, const StagedOut& out, int n, f
   if (NB == 1) w4 ? launch_staged_nb<FMT_W4A16, 1>(a, p.grid, p.smem, xy, st) : launch_staged_nb<FMT_BF16, 1>(a, p.grid, p.smem, xy, st);
   else if (NB == 2) w4 ? launch_staged_nb<FMT_W4A16, 2>(a, p.grid, p.smem, xy, st) : launch_staged_nb<FMT_BF16, 2>(a, p.grid, p.smem, xy, st);
   else w4 ? launch_staged_nb<FMT_W4A16, 4>(a, p.grid, p.smem, xy, st) : launch_staged_nb<FMT_BF16, 4>(a, p.grid, p.smem, xy, st);
+  return true;
+}
+
+// The vocabulary projection with the greedy choice (EPI_ARGMAX of gemv_s.cuh) on the staged
+// kernel: one K slice, one CTA per SM taking row blocks until none is left, and as many ring
+// slots as the opt-in shared memory holds (it is the step's last kernel and the longest
+// stream: the more weight bytes in flight per SM, the closer to the HBM rate).  By default it
+// takes the W4A16 vocabulary table (E2B, batch 1: 226 MB in place of the GEMV's three CTAs
+// per SM at 160 registers); a bf16 table stays on the persistent GEMV, which streamed it
+// faster.  The environment G4_LMHEAD_STAGED=0 keeps both on the GEMV, =1 puts both on the
+// staged kernel (for comparisons).
+bool lmhead_staged(int fmt) {
+  static const int mode = [] {
+    const char* e = getenv("G4_LMHEAD_STAGED");
+    return e ? (e[0] == '0' ? 0 : 1) : 2;
+  }();
+  return mode == 1 || (mode == 2 && fmt == G4_W4A16);
+}
+SPlan plan_staged_argmax(const Lin& L, int NB, int norm_n, int sms, int smem_max) {
+  SPlan p;
+  const bool w4 = L.fmt == G4_W4A16;
+  const int sgb = 8 * 512 + (w4 ? 512 : 0);
+  GemvSArgs& a = p.a;
+  a.C = 1;
+  a.spc = L.S;
+  a.cap = L.n_rb;
+  a.am = 1;
+  a.csg = std::max(1, std::min({a.spc, kSgMaxCsg, 32768 / sgb}));
+  a.slot_bytes = (a.csg * sgb + 127) / 128 * 128;
+  a.pro = PRO_RESID;
+  a.norm_n = norm_n;
+  const int nch = cdiv(a.spc, a.csg);
+  for (a.slots = kSgMaxSlots;; --a.slots) {
+    a.ru = cdiv(a.slots, nch) + 2;  // ru * nch > slots + nch: a unit slot is free when reused
+    p.smem = (size_t)sg_smem_plan(NB, 1, sgk(L.fmt), a).total + 128;
+    if ((int)p.smem <= smem_max || a.slots <= 2) break;
+  }
+  p.grid = sms;
+  p.ok = (int)p.smem <= smem_max && a.ru <= kSgMaxUnits && a.slots >= 2;
+  return p;
+}
+template <int FMT, int NB>
+void launch_staged_argmax_nb(const GemvSArgs& a, int grid, size_t smem, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSgThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, gemv_s_kernel<FMT, 1, NB, EPI_ARGMAX>, a);
+}
+// logits = W x (optional, [n][logits_stride]) and next_ids[b] = argmax_n logits[b][n] for the
+// residual-prologue input `in`.  am_val / am_idx: n * sms entries; am_cnt: zero, left zero.
+// False if the projection has no such plan (the caller uses the GEMV).
+bool run_staged_argmax(const Lin& L, const StagedIn& in, float* logits, int logits_stride, int* next_ids, int n,
+                       float eps, int* err, unsigned* ctr, float* am_val, int* am_idx, unsigned* am_cnt, int sms,
+                       int smem_max, cudaStream_t st) {
+  if (L.R != 1 || in.pro != PRO_RESID || n < 1 || n > kMaxNB) return false;
+  const int NB = n == 1 ? 1 : (n == 2 ? 2 : 4);
+  SPlan p = plan_staged_argmax(L, NB, L.K, sms, smem_max);
+  if (!p.ok) return false;
+  GemvSArgs& a = p.a;
+  a.qw = L.qw;
+  a.sc = L.sc;
+  a.n_rb = L.n_rb;
+  a.S = L.S;
+  a.tiles = L.tiles;
+  a.K = L.K;
+  a.n_valid = L.n_valid;
+  a.grab = ctr;
+  a.done = ctr + kSgMaxParts;
+  a.nb = n;
+  a.x_in = in.x;
+  a.x_stride = in.x_stride;
+  a.x_parts = 1;
+  a.r_in = in.r;
+  a.r_stride = in.r_stride;
+  a.r_parts = in.r_parts;
+  a.r_part_stride = in.r_part_stride;
+  a.g_r = in.g_r;
+  a.lambda = in.lambda;
+  a.g_a = in.g_a;
+  a.x_out = in.x_out;
+  a.eps = eps;
+  a.y = logits;
+  a.y_stride = logits_stride;
+  a.err = err;
+  a.am_val = am_val;
+  a.am_idx = am_idx;
+  a.am_cnt = am_cnt;
+  a.next_ids = next_ids;
+  const bool w4 = L.fmt == G4_W4A16;
+  if (NB == 1) w4 ? launch_staged_argmax_nb<FMT_W4A16, 1>(a, p.grid, p.smem, st) : launch_staged_argmax_nb<FMT_BF16, 1>(a, p.grid, p.smem, st);
+  else if (NB == 2) w4 ? launch_staged_argmax_nb<FMT_W4A16, 2>(a, p.grid, p.smem, st) : launch_staged_argmax_nb<FMT_BF16, 2>(a, p.grid, p.smem, st);
+  else w4 ? launch_staged_argmax_nb<FMT_W4A16, 4>(a, p.grid, p.smem, st) : launch_staged_argmax_nb<FMT_BF16, 4>(a, p.grid, p.smem, st);
   return true;
 }
 
@@ -1126,8 +1230,29 @@ g4_status run_step_staged(g4_handle* h, cudaStream_t st, int n, const int* d_slo
       TRY(staged(Y.pp, in, h->sq_rple, H, ps_h, &rple_parts, "gemv.ple_proj"));
     }
   }
-  {  // final norm, lm_head, argmax (K-split GEMV; the branch comes in parts)
+  {  // final norm, lm_head, argmax (the branch comes in parts)
     const Layer& Pv = h->layers[L - 1];
+    float* x_fin = next_x();
+    bool done = false;
+    if (lmhead_staged(h->lm.fmt)) {
+      StagedIn in;
+      in.pro = PRO_RESID;
+      in.x = cur;
+      in.x_stride = H;
+      in.r = h->sq_rple;
+      in.r_stride = H;
+      in.r_parts = rple_parts;
+      in.r_part_stride = ps_h;
+      in.g_r = Pv.post_ple_norm;
+      in.lambda = Pv.lambda;
+      in.g_a = h->g_final;
+      in.x_out = x_fin;
+      ProfScope ps(prof, "gemv.lm_head_argmax", (double)h->lm.bytes);
+      // the persistent GEMV's argmax counter (one past its row-group counters) is idle here
+      unsigned* am_cnt = h->gemv_cnt + (size_t)(h->lm.n_rb / h->lm.R) * h->lm.ksplit;
+      done = run_staged_argmax(h->lm, in, d_logits, c.vocab, d_next, n, eps, h->err, ctr(), h->am_val, h->am_idx,
+                               am_cnt, h->sms, h->smem_optin, st);
+    }
     GemvIO io;
     io.pro = PRO_RESID;
     io.x_in = cur;
@@ -1140,12 +1265,12 @@ g4_status run_step_staged(g4_handle* h, cudaStream_t st, int n, const int* d_slo
     io.g_r = Pv.post_ple_norm;
     io.lambda = Pv.lambda;
     io.g_a = h->g_final;
-    io.x_out = next_x();
+    io.x_out = x_fin;
     io.logits = d_logits;
     io.logits_stride = c.vocab;
     io.next_ids = d_next;
     Scratch s{h->gemv_part, h->gemv_cnt, h->am_val, h->am_idx, h->err};
-    {
+    if (!done) {
       ProfScope ps(prof, "gemv.lm_head_argmax", (double)h->lm.bytes);
       run_gemv(h->lm, EPI_ARGMAX, io, n, eps, s, h->sms, st, nullptr);
     }
@@ -2074,10 +2199,11 @@ g4_status g4_create(const g4_config* cfg, const g4_weights* weights, int device,
   if (v != G4_OK) return v;
   if (!weights) return G4_ERR_INVALID_ARG;
   DEVICE_GUARD(device);
-  init_kernel_attrs(device);
+  const int optin = init_kernel_attrs(device);
   g4_handle* h = new g4_handle();
   h->cfg = *cfg;
   h->device = device;
+  h->smem_optin = optin;
   if (const char* fa = getenv("G4_FAIL_ALLOC_AT")) h->fail_at = atoi(fa);
   cudaError_t e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, device);
   if (!cuda_ok(e, "cudaDeviceGetAttribute")) { delete h; return G4_ERR_CUDA; }

@@ -22,6 +22,16 @@
 // Dequantisation and accumulation are those of the GEMV (tile_fma): bf16(q * s) weights,
 // fp32 activations and sums.  Every wait is bounded; on expiry the CTA sets the device error
 // word, stops, and waits (bounded) for the copies it issued before it exits.
+//
+// EPI_ARGMAX (the vocabulary projection and greedy choice, one K slice): a CTA takes as many
+// row groups as its speed allows, so their sums cannot all stay in shared memory.  They go to
+// a ring of `ru` unit slots instead; the warp that finishes a row group last (a shared-memory
+// counter per slot) adds the eight warps' sums in warp order, writes the logits (if asked
+// for) and keeps a running best per lane.  A slot is reused `ru` row groups later, which no
+// warp reaches before that reduction is over (the ring of weights keeps the warps within
+// `slots` items of one another, and ru * items per row group > slots + items per row group).
+// The CTA's best goes to am_val / am_idx, and the last CTA to finish picks the winner
+// (lowest index on ties, NaN never wins) into next_ids.
 #pragma once
 #include "common.cuh"
 #include "gemm_tc.cuh"
@@ -76,11 +86,18 @@ struct GemvSArgs {
   const float* ple;  // PRO_PLEG: multipliers [nb][ple_stride]
   int ple_stride;
   int* err;
+  // units whose sums shared memory holds: cap, or (EPI_ARGMAX) the ring of unit slots
+  int ru;
+  int am;          // 1: EPI_ARGMAX layout (per-slot counters in shared memory)
+  float* am_val;   // EPI_ARGMAX: per-CTA bests [nb][grid]
+  int* am_idx;
+  unsigned* am_cnt;  // CTAs done; zero before the launch, left zero after it
+  int* next_ids;     // [nb]
 };
 
 // Shared-memory plan (bytes from a 128-aligned base), identical on host and device.
-//   ring | barriers, slot tags, unit rows, flags | xs [NB][kc] |
-//   stage (x rows, r rows, two gain vectors) | red [cap][warps][NV] | norm scratch [32][4 NB]
+//   ring | barriers, slot tags, unit rows, flags, (EPI_ARGMAX) slot counters | xs [NB][kc] |
+//   stage (x rows, r rows, two gain vectors) | red [ru][warps][NV] | norm scratch [32][4 NB]
 struct SgSmem {
   int bars, tags, units, xs, stage, red, nred, total;
 };
@@ -93,14 +110,15 @@ __host__ __device__ inline SgSmem sg_smem_plan(int NB, int R, int sgk, const Gem
   p.tags = o;
   o += a.slots * 4;            // unit of each slot's item (-1: no more)
   p.units = o;
-  o += kSgMaxUnits * 4 + 16;   // row group of each unit; abort and fail flags
+  o += kSgMaxUnits * 4 + 16;   // row group of each unit; abort, fail and last-CTA flags
+  if (a.am) o += kSgMaxUnits * 4;  // warps done with each unit slot
   o = (o + 15) & ~15;
   p.xs = o;
   o += NB * a.spc * sgk * 4;
   p.stage = o;
   if (a.pro != PRO_PLAIN) o += (2 * NB * a.norm_n + a.norm_n) * 4;
   p.red = o;
-  o += a.cap * kSgWarps * nv * 4;
+  o += a.ru * kSgWarps * nv * 4;
   p.nred = o;
   o += 32 * 4 * NB * 4;
   p.total = o;
@@ -435,9 +453,11 @@ __global__ void __maxnreg__(kSgMaxRegs) gemv_s_kernel(const GemvSArgs a) {
   uint64_t* empty = full + a.slots;
   uint64_t* done = empty + a.slots;               // the compute warps have finished (producer drain)
   volatile int* tag = reinterpret_cast<volatile int*>(smem + L.tags);     // [slots] unit of the item
-  volatile int* unit_rg = reinterpret_cast<volatile int*>(smem + L.units);  // [kSgMaxUnits]
+  volatile int* unit_rg = reinterpret_cast<volatile int*>(smem + L.units);  // [ru] row group of a unit slot
   volatile int* abort_s = unit_rg + kSgMaxUnits;  // tells the producer to stop
   volatile int* cfail = abort_s + 1;              // compute warps: written before a barrier, read after it
+  volatile int* am_last = abort_s + 2;            // EPI_ARGMAX: this CTA finished last
+  unsigned* ucnt = reinterpret_cast<unsigned*>(const_cast<int*>(abort_s + 4));  // EPI_ARGMAX: [ru]
   float* xs = reinterpret_cast<float*>(smem + L.xs);
   float* stage = reinterpret_cast<float*>(smem + L.stage);
   float* red = reinterpret_cast<float*>(smem + L.red);  // [cap][warps][NV]
@@ -461,6 +481,8 @@ __global__ void __maxnreg__(kSgMaxRegs) gemv_s_kernel(const GemvSArgs a) {
     mbar_init(done, 1);
     *abort_s = 0;
     *cfail = 0;
+    if constexpr (EPI == EPI_ARGMAX)
+      for (int i = 0; i < a.ru; ++i) ucnt[i] = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -485,7 +507,7 @@ __global__ void __maxnreg__(kSgMaxRegs) gemv_s_kernel(const GemvSArgs a) {
         if (!slot_free(it % a.slots, it / a.slots)) { dead = true; break; }
         const int rg = (int)atomicAdd(&a.grab[ks], 1u);
         if (rg >= n_rg) break;
-        unit_rg[u] = rg;
+        unit_rg[u % a.ru] = rg;
         for (int c = 0; c < nch; ++c, ++it) {
           const int s = it % a.slots, ph = it / a.slots;
           if (c > 0 && !slot_free(s, ph)) { dead = true; break; }
@@ -542,6 +564,10 @@ __global__ void __maxnreg__(kSgMaxRegs) gemv_s_kernel(const GemvSArgs a) {
   int units = 0;
   bool ok = true;
   float2 acc[R][NB];
+  float best_v[NB];  // EPI_ARGMAX: running best of this lane's rows
+  int best_i[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) { best_v[b] = __int_as_float(0x7fc00000); best_i[b] = 0x7fffffff; }
   for (int it = 0; ok; ++it) {
     const int s = it % a.slots, ph = it / a.slots;
     if (!sg_wait(&full[s], ph & 1, nullptr)) {
@@ -590,8 +616,46 @@ __global__ void __maxnreg__(kSgMaxRegs) gemv_s_kernel(const GemvSArgs a) {
       }
     }
     __syncwarp();
+    if constexpr (EPI == EPI_ARGMAX) {
+      // the unit's reduction comes before this warp releases the slot (see the header)
+      if (c == nch - 1) {
+        const int us = u % a.ru;
+        float* rb = red + (size_t)us * kSgWarps * NV;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int b = 0; b < NB; ++b) rb[warp * NV + (r * NB + b) * 32 + lane] = acc[r][b].x + acc[r][b].y;
+        __syncwarp();
+        unsigned prev = 0;
+        if (lane == 0) {
+          __threadfence_block();
+          prev = atomicAdd(&ucnt[us], 1u);
+        }
+        prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+        if (prev == (unsigned)kSgWarps - 1) {  // the other warps' sums are in
+          __threadfence_block();
+          const int rg = unit_rg[us];
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const int n = (rg * R + r) * 32 + lane;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+              float v = 0.f;
+#pragma unroll
+              for (int w = 0; w < kSgWarps; ++w) v += rb[w * NV + (r * NB + b) * 32 + lane];
+              if (n < a.n_valid && b < a.nb) {
+                if (a.y) a.y[(size_t)b * a.y_stride + n] = v;
+                if (argmax_better(v, n, best_v[b], best_i[b])) { best_v[b] = v; best_i[b] = n; }
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) ucnt[us] = 0u;
+        }
+      }
+    }
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (c == nch - 1) {
+    if (EPI != EPI_ARGMAX && c == nch - 1) {
       // this warp's sums of unit u (its own slot: no barrier between row groups)
       float* rb = red + (size_t)u * kSgWarps * NV;
 #pragma unroll
@@ -603,6 +667,54 @@ __global__ void __maxnreg__(kSgMaxRegs) gemv_s_kernel(const GemvSArgs a) {
   }
   sg_csync();
   if (*cfail) return;
+  if constexpr (EPI == EPI_ARGMAX) {
+    // the CTA's best per batch row, then the grid's (last CTA), in index order on ties
+    float* av = nred;
+    int* ai = reinterpret_cast<int*>(nred + NB * kSgWarps);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      float v = best_v[b];
+      int i = best_i[b];
+      warp_argmax(v, i);
+      if (lane == 0) { av[b * kSgWarps + warp] = v; ai[b * kSgWarps + warp] = i; }
+    }
+    sg_csync();
+    if (threadIdx.x == 0) {
+      for (int b = 0; b < a.nb; ++b) {
+        float v = av[b * kSgWarps];
+        int i = ai[b * kSgWarps];
+        for (int w = 1; w < kSgWarps; ++w)
+          if (argmax_better(av[b * kSgWarps + w], ai[b * kSgWarps + w], v, i)) { v = av[b * kSgWarps + w]; i = ai[b * kSgWarps + w]; }
+        a.am_val[b * gridDim.x + blockIdx.x] = v;
+        a.am_idx[b * gridDim.x + blockIdx.x] = i;
+      }
+      __threadfence();
+      *am_last = atomicAdd(a.am_cnt, 1u) == gridDim.x - 1;
+    }
+    sg_csync();
+    if (!*am_last) return;
+    __threadfence();
+    for (int b = 0; b < a.nb; ++b) {
+      float v = __int_as_float(0x7fc00000);
+      int i = 0x7fffffff;
+      for (int cta = threadIdx.x; cta < (int)gridDim.x; cta += kSgWarps * 32) {
+        const float cv = ldcg(a.am_val + b * gridDim.x + cta);
+        const int ci = __ldcg(a.am_idx + b * gridDim.x + cta);
+        if (argmax_better(cv, ci, v, i)) { v = cv; i = ci; }
+      }
+      warp_argmax(v, i);
+      if (lane == 0) { av[warp] = v; ai[warp] = i; }
+      sg_csync();
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < kSgWarps; ++w)
+          if (argmax_better(av[w], ai[w], av[0], ai[0])) { av[0] = av[w]; ai[0] = ai[w]; }
+        a.next_ids[b] = ai[0] == 0x7fffffff ? 0 : ai[0];
+      }
+      sg_csync();
+    }
+    if (threadIdx.x == 0) *a.am_cnt = 0u;
+    return;
+  }
   // outputs: value v = (r * NB + b) * 32 + lane of unit u is row (rg * R + r) * 32 + lane of
   // batch row b, summed over the warps in warp order
   float* ys = a.y + (size_t)ks * a.y_part_stride;

@@ -375,7 +375,7 @@ def run_gpu(args, wl, cfg, fmt):
                    "l2": "inputs larger than L2 (weights streamed every step exceed 129 MB)",
                    "seed": args.seed,
                    "knobs": {k: os.environ[k] for k in ("G4_TC_MIN_BATCH", "G4_GEMV_UNSPLIT_BYTES", "G4_GEMV_STAGED",
-                                                        "G4_ATTN_MQA_MIN") if k in os.environ}},
+                                                        "G4_ATTN_MQA_MIN", "G4_LMHEAD_STAGED") if k in os.environ}},
         "roofline": {"bound": "hbm", "kernel": dom_name, "achieved": round(dom_bytes / (dom_ms / 1e3) / 1e9, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(dom_bytes / (dom_ms / 1e3) / 1e9 / peak, 4),
                      "traffic": (round(dom_bytes * MEASURED_TRAFFIC_RATIO[(fmt, dom_name)])

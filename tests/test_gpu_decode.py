@@ -209,6 +209,27 @@ def test_batch_larger_than_gemv_chunk(rt):
     assert np.max(np.abs(logits - ref["logits"])) <= LOGIT_TOL
 
 
+@pytest.mark.parametrize("batch", [1, 2, 3])
+def test_tokens_without_logits(rt, batch):
+    """The greedy choice of a decode step is the same whether or not the step also writes the
+    logits out (the vocabulary projection's argmax epilogue with and without its logits
+    store; int4 tables put it on the staged kernel), and matches the oracle's wherever its
+    top-2 gap is clear."""
+    cfg = synth.get_config("e2b-v8k")
+    w = synth.make_model_weights(cfg, "w4a16", seed=1, tables="int4")
+    prompts = list(synth.make_prompts(cfg["vocab"], batch, 20, seed=1))
+    ref = oracle.Oracle(cfg, w, max_batch=batch, max_context=64).generate(np.asarray(prompts), 6, keep_logits=True)
+    runs = []
+    for want in (True, False):
+        dec = rt.Decoder(cfg, w, max_batch=batch, max_context=64)
+        runs.append(gpu_generate(dec, prompts, 6, teacher=ref["tokens"], want_logits=want)[0])
+        assert dec.device_error()[1] == 0
+        dec.close()
+    assert np.array_equal(runs[0], runs[1])
+    ok = ref["gaps"].T > GAP_TIE
+    assert np.all((runs[1] == ref["tokens"]) | ~ok)
+
+
 def test_rerun_is_bitwise_deterministic(rt):
     cfg = synth.get_config("tiny")
     w = synth.make_weights(cfg, "w4a16", seed=1)

@@ -1,7 +1,9 @@
 """Launch-planning knobs against the oracle, each in a fresh process (the library reads them
 once per process): with G4_GEMV_STAGED=0 and G4_GEMV_UNSPLIT_BYTES set above every
 projection's size, every batch-1 projection runs on the one-slice GEMV (its GeGLU, per-layer
-and argmax epilogues at E2B widths); G4_TC_MIN_BATCH=0 keeps batch 8 on the GEMV; and
+and argmax epilogues at E2B widths); G4_LMHEAD_STAGED=1 puts the bf16 vocabulary projection of
+a staged step on the staged kernel's argmax epilogue; G4_TC_MIN_BATCH=0 keeps batch 8 on the
+GEMV; and
 G4_ATTN_MQA_MIN=0 keeps batch 8 on the per-head attention kernel.
 
 Seed 1: on these shapes the fp32 oracle stays within 2e-6 of an fp64 run (some seeds do not:
@@ -45,6 +47,7 @@ print(json.dumps({"max_d": float(np.max(np.abs(logits - ref["logits"]))), "err":
 @pytest.mark.parametrize("env,batch", [
     ({"G4_GEMV_STAGED": "0", "G4_GEMV_UNSPLIT_BYTES": "1000000000000"}, 1),
     ({"G4_GEMV_STAGED": "0"}, 2),
+    ({"G4_LMHEAD_STAGED": "1"}, 3),
     ({"G4_TC_MIN_BATCH": "0", "G4_ATTN_MQA_MIN": "0"}, 8),
 ])
 def test_knob_matches_oracle(env, batch):
